@@ -1,0 +1,182 @@
+"""ctypes wrapper of the fp64 C oracle (``mla_oracle.c``).
+
+TEST INFRASTRUCTURE ONLY.  Inputs are numpy arrays of float64, or of uint16
+holding raw bf16 bit patterns (widened exactly inside the C code).  Outputs
+are float64 numpy arrays.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "mla_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+F64 = 0
+BF16 = 1
+
+
+def build(force: bool = False) -> str:
+    """Compile ``liboracle.so`` with gcc + OpenMP (plain C, -O2, no fast-math)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(
+            ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-fno-fast-math",
+             "-ffp-contract=off", _SRC, "-o", tmp, "-lm"]
+        )
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB)
+        vp, i32, i64, f64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_double
+        lib.mla_oracle_num_threads.restype = i32
+        lib.mla_oracle_rope.argtypes = [vp, i32, vp, i32, i32, f64, vp]
+        lib.mla_oracle_decode.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32,
+                                          i32, i32, i32, i32, f64, f64, vp, i64, vp, vp]
+        lib.mla_oracle_absorb.argtypes = [vp, vp, i32, i32, i32, i32, i32, vp]
+        lib.mla_oracle_up_project.argtypes = [vp, vp, i32, i32, i32, i32, i32, vp]
+        lib.mla_oracle_latent_attention.argtypes = [vp, vp, vp, i32, vp, i32, i32, i32, i32,
+                                                    i32, i32, f64, vp, i64, vp]
+        for name in ("mla_oracle_rope", "mla_oracle_decode", "mla_oracle_absorb",
+                     "mla_oracle_up_project", "mla_oracle_latent_attention"):
+            getattr(lib, name).restype = i32
+        _lib = lib
+    return _lib
+
+
+def num_threads() -> int:
+    return int(load().mla_oracle_num_threads())
+
+
+def _arr(x, dtype_code=None):
+    """Return (contiguous array, dtype code).  uint16 means raw bf16 bits."""
+    a = np.ascontiguousarray(x)
+    if a.dtype == np.uint16:
+        code = BF16
+    elif a.dtype == np.float64:
+        code = F64
+    else:
+        raise TypeError(f"oracle inputs must be float64 or uint16 (bf16 bits), got {a.dtype}")
+    if dtype_code is not None and code != dtype_code:
+        raise TypeError("all oracle inputs of one call must share one dtype")
+    return a, code
+
+
+def _ptr(a):
+    return ctypes.c_void_p(a.ctypes.data)
+
+
+def _check(rc, what):
+    if rc != 0:
+        raise ValueError(f"oracle {what} failed with code {rc}")
+
+
+def rope(x, pos, base: float = 10000.0):
+    """RoPE of x[n, d_r] at integer positions pos[n] (interleaved pairs)."""
+    a, code = _arr(x)
+    n, d_r = a.shape
+    p = np.ascontiguousarray(pos, dtype=np.int64)
+    assert p.shape == (n,)
+    out = np.empty((n, d_r), np.float64)
+    _check(load().mla_oracle_rope(_ptr(a), code, _ptr(p), n, d_r, base, _ptr(out)), "rope")
+    return out
+
+
+def decode(q_nope, q_rope, c_kv, k_r, W_UK, W_UV, seqlens, *, softmax_scale=None,
+           rope_base: float = 10000.0, rows=None, return_wsum: bool = False):
+    """Unabsorbed MLA decode.  Shapes: q_nope [B,S,H,d_h], q_rope [B,S,H,d_r],
+    c_kv [B,Lmax,d_c], k_r [B,Lmax,d_r] (pre-RoPE), W_UK [H,d_h,d_c],
+    W_UV [H,d_v,d_c], seqlens [B].  Returns out [n_rows, d_v] for the flat rows
+    (b*S+s)*H+h (all rows, shaped [B,S,H,d_v], when rows is None)."""
+    qn, code = _arr(q_nope)
+    qr, _ = _arr(q_rope, code)
+    ck, _ = _arr(c_kv, code)
+    kr, _ = _arr(k_r, code)
+    wk, _ = _arr(W_UK, code)
+    wv, _ = _arr(W_UV, code)
+    B, S, H, d_h = qn.shape
+    d_r = qr.shape[3]
+    Lmax, d_c = ck.shape[1], ck.shape[2]
+    d_v = wv.shape[1]
+    assert qr.shape == (B, S, H, d_r) and ck.shape == (B, Lmax, d_c)
+    assert kr.shape == (B, Lmax, d_r) and wk.shape == (H, d_h, d_c) and wv.shape == (H, d_v, d_c)
+    sl = np.ascontiguousarray(seqlens, dtype=np.int32)
+    assert sl.shape == (B,)
+    if softmax_scale is None:
+        softmax_scale = 1.0 / np.sqrt(d_h + d_r)
+    if rows is None:
+        n_rows, rp = B * S * H, None
+    else:
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        n_rows, rp = rows.shape[0], _ptr(rows)
+    out = np.empty((n_rows, d_v), np.float64)
+    wsum = np.empty((n_rows,), np.float64)
+    rc = load().mla_oracle_decode(_ptr(qn), _ptr(qr), _ptr(ck), _ptr(kr), _ptr(wk), _ptr(wv),
+                                  code, _ptr(sl), B, S, H, Lmax, d_c, d_h, d_r, d_v,
+                                  float(softmax_scale), float(rope_base), rp, n_rows,
+                                  _ptr(out), _ptr(wsum))
+    _check(rc, "decode")
+    if rows is None:
+        out = out.reshape(B, S, H, d_v)
+        wsum = wsum.reshape(B, S, H)
+    return (out, wsum) if return_wsum else out
+
+
+def absorb(q_nope, W_UK):
+    """q~[n,h,:] = W_UK[h]^T q_nope[n,h,:].  q_nope [N,H,d_h], W_UK [H,d_h,d_c]."""
+    qn, code = _arr(q_nope)
+    wk, _ = _arr(W_UK, code)
+    N, H, d_h = qn.shape
+    d_c = wk.shape[2]
+    assert wk.shape == (H, d_h, d_c)
+    out = np.empty((N, H, d_c), np.float64)
+    _check(load().mla_oracle_absorb(_ptr(qn), _ptr(wk), code, N, H, d_h, d_c, _ptr(out)), "absorb")
+    return out
+
+
+def up_project(o_lat, W_UV):
+    """out[n,h,:] = W_UV[h] o_lat[n,h,:].  o_lat [N,H,d_c], W_UV [H,d_v,d_c]."""
+    ol, code = _arr(o_lat)
+    wv, _ = _arr(W_UV, code)
+    N, H, d_c = ol.shape
+    d_v = wv.shape[1]
+    assert wv.shape == (H, d_v, d_c)
+    out = np.empty((N, H, d_v), np.float64)
+    _check(load().mla_oracle_up_project(_ptr(ol), _ptr(wv), code, N, H, d_v, d_c, _ptr(out)),
+           "up_project")
+    return out
+
+
+def latent_attention(q_cat, c_kv, k_rot, seqlens, *, d_r: int, softmax_scale, rows=None):
+    """Absorbed latent attention o_lat for already rotated inputs.
+    q_cat [B,S,H,d_c+d_r], c_kv [B,Lmax,d_c], k_rot [B,Lmax,d_r]."""
+    qc, code = _arr(q_cat)
+    ck, _ = _arr(c_kv, code)
+    kr, _ = _arr(k_rot, code)
+    B, S, H, dq = qc.shape
+    Lmax, d_c = ck.shape[1], ck.shape[2]
+    assert dq == d_c + d_r and kr.shape == (B, Lmax, d_r)
+    sl = np.ascontiguousarray(seqlens, dtype=np.int32)
+    if rows is None:
+        n_rows, rp = B * S * H, None
+    else:
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        n_rows, rp = rows.shape[0], _ptr(rows)
+    out = np.empty((n_rows, d_c), np.float64)
+    rc = load().mla_oracle_latent_attention(_ptr(qc), _ptr(ck), _ptr(kr), code, _ptr(sl), B, S,
+                                            H, Lmax, d_c, d_r, float(softmax_scale), rp, n_rows,
+                                            _ptr(out))
+    _check(rc, "latent_attention")
+    if rows is None:
+        out = out.reshape(B, S, H, d_c)
+    return out
