@@ -1,0 +1,331 @@
+#!/usr/bin/env python3
+"""Benchmark of one MLA decode step (absorb -> RoPE -> latent decode ->
+split-KV combine -> up-projection) on B300.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                  [--impl ours|reference] [--quick]
+
+Prints ONE JSON line (rank 0).  ``value`` is device time per step (us, lower
+is better) with all inputs resident in HBM and L2 flushed between steps;
+``e2e`` is the same step through the C ABI from pinned host buffers (query in,
+output back) per step.  ``--impl reference`` times the fp64 CPU oracle on a
+bounded sample of the same workload instead.  Under torchrun every rank runs
+an independent replica (no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from mla_latent_kv_68_b300.inputs import WORKLOADS, bf16_bits, workload_inputs  # noqa: E402
+
+METRIC = "MLA decode µs/step, cache GB/s and TFLOP/s as fraction of B300 roofline"
+DEFAULT_WORKLOAD = "uniform_b32_s1_h128_l4096"
+CACHE_BYTES_PER_TOKEN = (512 + 64) * 2
+FLOPS_PER_VISIBLE_TOKEN_PER_HEAD = 2 * 576 + 2 * 512
+L2_FLUSH_BYTES = 256 << 20
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        return 6400.0, 1800.0, 1400.0, "fallback"
+
+
+def _work(x):
+    """Algorithmic bytes and flops of the decode kernel and of the whole step."""
+    B, S, H = x["B"], x["S"], x["H"]
+    L = x["seqlens"].to(torch.int64)
+    cache = int(L.sum()) * CACHE_BYTES_PER_TOKEN
+    vis = int(sum(int(l) - S + s + 1 for l in L.tolist() for s in range(S)))
+    rows = B * S * H
+    dec_bytes = cache + rows * 576 * 2 + rows * 512 * 2          # cache + q_cat in + o_lat out
+    dec_flops = vis * H * FLOPS_PER_VISIBLE_TOKEN_PER_HEAD
+    w_bytes = 2 * H * 128 * 512 * 2
+    step_bytes = dec_bytes + w_bytes + rows * (128 + 64 + 128) * 2
+    step_flops = dec_flops + 2 * (2 * rows * 128 * 512)
+    return dict(dec_bytes=dec_bytes, dec_flops=dec_flops, step_bytes=step_bytes,
+                step_flops=step_flops, cache_bytes=cache)
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during timing."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def _oracle_sample(x, seconds: float, seed: int = 0):
+    """Time the oracle on a bounded random sample of output rows; return the
+    extrapolated whole-step time in us, the thread count and the sample text."""
+    import oracle
+    threads = oracle.num_threads()
+    b = {k: bf16_bits(x[k]) for k in ("q_nope", "q_rope", "c_kv", "k_r", "W_UK", "W_UV")}
+    total = x["B"] * x["S"] * x["H"]
+    rng = np.random.default_rng(seed)
+    L = x["seqlens"].numpy().astype(np.int64)
+    per_row_tokens = np.repeat(L, x["S"] * x["H"]).astype(np.float64)
+    # probe one batch of `threads` rows, then size the sample to about `seconds`
+    n = min(total, threads)
+    rows = rng.choice(total, n, replace=False)
+    t0 = time.perf_counter()
+    oracle.decode(b["q_nope"], b["q_rope"], b["c_kv"], b["k_r"], b["W_UK"], b["W_UV"],
+                  x["seqlens"].numpy(), rows=rows)
+    dt = time.perf_counter() - t0
+    if dt < seconds and n < total:
+        n2 = int(min(total, max(n, n * seconds / max(dt, 1e-3))))
+        rows = rng.choice(total, n2, replace=False)
+        t0 = time.perf_counter()
+        oracle.decode(b["q_nope"], b["q_rope"], b["c_kv"], b["k_r"], b["W_UK"], b["W_UV"],
+                      x["seqlens"].numpy(), rows=rows)
+        dt = time.perf_counter() - t0
+        n = n2
+    # extrapolate by visible tokens (the oracle's cost is linear in them)
+    frac = per_row_tokens[rows].sum() / per_row_tokens.sum()
+    us = dt / frac * 1e6
+    return us, threads, (f"{n} of {total} output rows (random, seeded), {dt:.1f} s wall; "
+                         f"scaled by visible-token share {frac:.4f}")
+
+
+def run_reference(args, x, rank, world):
+    if rank != 0:
+        return
+    per_step = []
+    for i in range(args.warmup + args.steps):
+        us, threads, sample = _oracle_sample(x, seconds=args.ref_seconds, seed=i)
+        if i >= args.warmup:
+            per_step.append(us)
+    v = statistics.mean(per_step)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(v, 3), "unit": "us/step",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(v / 1000, 3), "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": _config(args, x),
+        "cpu_baseline": {"value": round(v, 3), "unit": "us/step", "cores": threads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(v, 3), "unit": "us/step", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def _config(args, x):
+    w = WORKLOADS[args.workload]
+    return {"workload": args.workload, "B": w.B, "S": w.S, "H": w.H,
+            "L": w.L if w.L is not None else f"U[{w.L_range[0]},{w.L_range[1]}]",
+            "sum_L": int(x["seqlens"].sum()), "d_c": 512, "d_rope": 64,
+            "l2": "flushed between timed steps (256 MiB write)",
+            "parallelism": f"replicas x{args.gpus}" if args.gpus > 1 else "single GPU"}
+
+
+def run_ours(args, x, rank, world, local_rank):
+    from mla_latent_kv_68_b300 import binding as mb
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    mb.lib()
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    mb.rope_cache(d["k_r"], d["seqlens"])          # cache fill: keys rotated once (untimed)
+    step = mb.DecodeStep(x["B"], x["S"], x["H"], device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    args_step = (d["q_nope"], d["q_rope"], d["c_kv"], d["k_r"], d["seqlens"], d["W_UK"], d["W_UV"])
+
+    for _ in range(args.warmup):
+        step(*args_step)
+    if mb.read_status(step.workspace) != mb.MLA_OK:
+        raise RuntimeError("device status not clean after warm-up")
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    _barrier(world)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local_rank) as clocks:
+        for i in range(args.steps):
+            flush.zero_()
+            e = ev[i]
+            e[0].record(stream)
+            mb.absorb_q(d["q_nope"], d["W_UK"], step.q_cat)
+            mb.rope_queries(d["q_rope"], step.q_cat, d["seqlens"])
+            e[1].record(stream)
+            mb.decode(step.q_cat, d["c_kv"], d["k_r"], d["seqlens"], step.workspace)
+            e[2].record(stream)
+            mb.splitkv_combine(step.workspace, step.o_lat)
+            mb.up_project(step.o_lat, d["W_UV"], step.out)
+            e[3].record(stream)
+        torch.cuda.synchronize(dev)
+    _barrier(world)
+    if mb.read_status(step.workspace) != mb.MLA_OK:
+        raise RuntimeError("device status not clean after the timed steps")
+    step_ms = [e[0].elapsed_time(e[3]) for e in ev]
+    dec_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    step_us = _max_over_ranks(statistics.mean(step_ms) * 1000, world)
+    dec_us = _max_over_ranks(statistics.mean(dec_ms) * 1000, world)
+
+    # end to end through the C ABI from pinned host buffers (query in, output back)
+    hq = x["q_nope"].pin_memory()
+    hr = x["q_rope"].pin_memory()
+    hl = x["seqlens"].pin_memory()
+    hout = torch.empty(step.out.shape, dtype=torch.bfloat16).pin_memory()
+    q_dev, r_dev, l_dev = torch.empty_like(d["q_nope"]), torch.empty_like(d["q_rope"]), torch.empty_like(d["seqlens"])
+    h2d = hq.numel() * 2 + hr.numel() * 2 + hl.numel() * 4
+    d2h = hout.numel() * 2
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.zero_()
+        e2e_ev[i][0].record(stream)
+        q_dev.copy_(hq, non_blocking=True)
+        r_dev.copy_(hr, non_blocking=True)
+        l_dev.copy_(hl, non_blocking=True)
+        step(q_dev, r_dev, d["c_kv"], d["k_r"], l_dev, d["W_UK"], d["W_UV"])
+        hout.copy_(step.out, non_blocking=True)
+        e2e_ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_us = _max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in e2e_ev) * 1000, world)
+
+    if rank != 0:
+        return
+    hbm, tf_burst, tf_sust, src = _peaks()
+    wk = _work(x)
+    achieved = wk["dec_bytes"] / (dec_us * 1e-6) / 1e9
+    line = {
+        "metric": METRIC, "value": round(step_us, 3), "unit": "us/step", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_us / 1000, 5),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; random-init weights of the pages' MLA dimensions)",
+        "config": _config(args, x),
+        "roofline": {"kernel": "mla_decode (plan + decode kernels)", "bound": "hbm",
+                     "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(achieved / hbm, 4), "traffic": None,
+                     "peak_source": src,
+                     "tensor_tflops": round(wk["dec_flops"] / (dec_us * 1e-6) / 1e12, 1),
+                     "tensor_frac_of_burst": round(wk["dec_flops"] / (dec_us * 1e-6) / 1e12 / tf_burst, 4)},
+        "kernels": {"decode_us": round(dec_us, 3), "step_us": round(step_us, 3),
+                    "step_roofline_us": round(max(wk["step_bytes"] / (hbm * 1e3),
+                                                  wk["step_flops"] / (tf_burst * 1e6)), 3),
+                    "algorithmic_decode_bytes": wk["dec_bytes"],
+                    "algorithmic_decode_flops": wk["dec_flops"]},
+        "e2e": {"value": round(e2e_us, 3), "unit": "us/step", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": mb.DecodeStep.LAUNCHES_PER_STEP * args.steps,
+        "clocks": clocks.summary(),
+    }
+    if not args.quick and world == 1:
+        us, threads, sample = _oracle_sample(x, seconds=args.ref_seconds)
+        line["cpu_baseline"] = {"value": round(us, 1), "unit": "us/step", "cores": threads,
+                                "kind": "oracle", "sample": sample}
+    print(json.dumps(line), flush=True)
+
+
+def _barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def _max_over_ranks(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    t = torch.tensor([v], dtype=torch.float64,
+                     device="cuda" if torch.distributed.get_backend() == "nccl" else "cpu")
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--quick", action="store_true", help="skip the CPU-baseline timing")
+    ap.add_argument("--ref-seconds", type=float, default=12.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        if args.impl == "reference" and rank != 0:
+            return 0
+        if args.impl == "ours":
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+            if backend == "nccl":
+                torch.cuda.set_device(local_rank)
+            torch.distributed.init_process_group(backend)
+    x = workload_inputs(args.workload)
+    if args.impl == "reference":
+        run_reference(args, x, rank, world)
+    else:
+        run_ours(args, x, rank, world, local_rank)
+    if world > 1 and args.impl == "ours":
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

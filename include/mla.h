@@ -1,0 +1,169 @@
+/*
+ * mla.h -- C ABI of a B300 (sm_103a) library for the decode step of
+ * Multi-head Latent Attention (MLA) in its weight-absorbed form.
+ *
+ * The operation is the one of "DeepSeek-V3" (ekkoxiao.github.io), section
+ * "Multi-Head Latent Attention": every cached token holds a latent
+ * c^KV (d_c = 512) and a RoPE key k^R (d_h^R = 64) shared by all heads
+ * (sub-section "KeyValue"); a head i scores position j as
+ *     s = (q^C . W_i^UK c_j + q^R . k^R_j) / sqrt(d_h + d_h^R),   d_h = 128
+ * (sub-section "注意力计算"), which the sub-section "潜在向量的作用" rewrites as
+ *     q~ = (W_i^UK)^T q^C,   s = (q~ . c_j + q^R . k^R_j) / sqrt(192),
+ *     o = W_i^UV (sum_j a_j c_j)        with a = softmax_j(s).
+ * The dimensions are fixed by "DeepSeek-V3 技术报告精读" (oopvo.github.io),
+ * section "维度分解详解": qk_nope 128, qk_rope 64, v 128, kv_lora_rank 512.
+ *
+ * One decode step is five calls on one stream:
+ *   mla_absorb_q -> mla_rope_apply (queries) -> mla_decode
+ *   -> mla_splitkv_combine -> mla_up_project.
+ * The cache's k^R is rotated once, when it is written (mla_rope_apply on the
+ * cache), because the pages cache the rotated key.
+ *
+ * Conventions for every call:
+ *   - All tensor pointers are DEVICE pointers to row-major, contiguous data,
+ *     16-byte aligned.  bf16 values are passed as their 16-bit patterns.
+ *   - The caller owns all memory.  The library never allocates or frees
+ *     device memory and never synchronises, except in mla_read_status.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the
+ *     legacy default stream) and may be captured in a CUDA graph.
+ *   - Arguments are validated on the host first; on an error nothing is
+ *     launched and the status is returned at once.  Errors found on the
+ *     device (a sequence length out of range, a wait that timed out) are
+ *     recorded in the decode workspace and returned by mla_read_status.
+ *   - Query positions are 0-based: keys sit at 0..L_b-1 and query s of S at
+ *     L_b - S + s, which sees keys 0..L_b - S + s.
+ */
+#ifndef MLA_H
+#define MLA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t mla_bf16; /* raw bf16 bit pattern */
+
+typedef enum {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARG = 1, /* null pointer, misalignment, bad size or stride */
+  MLA_ERR_UNSUPPORTED = 2, /* a shape this build does not implement */
+  MLA_ERR_WORKSPACE = 3,   /* workspace missing or too small */
+  MLA_ERR_CUDA = 4,        /* a CUDA runtime call or a launch failed */
+  MLA_ERR_BAD_SEQLEN = 5,  /* device: some seqlens[b] < S or > Lmax */
+  MLA_ERR_TIMEOUT = 6      /* device: a bounded wait inside a kernel ran out */
+} mla_status;
+
+/* Fixed dimensions of the layout. */
+enum { MLA_D_C = 512, MLA_D_R = 64, MLA_D_QK = 576, MLA_D_H = 128, MLA_D_V = 128 };
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *mla_status_string(int status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int mla_version(void);
+
+/*
+ * Absorb the key up-projection into the query ("潜在向量的作用":
+ * q~_{b,s,h} = (W_h^UK)^T q^C_{b,s,h}).  fp32 accumulation on the tensor
+ * cores, result rounded to bf16.
+ *   q_nope [B,S,H,128]  bf16, the content query q^C
+ *   W_UK   [H,128,512]  bf16, W_UK[h][d][k] = row block h of W^UK
+ *   q_cat  [B,S,H,576]  bf16 output; columns 0..511 are written, 512..575
+ *                       are left untouched (mla_rope_apply fills them)
+ * Requires 1 <= H <= 128, B*S >= 1.
+ */
+mla_status mla_absorb_q(const mla_bf16 *q_nope, const mla_bf16 *W_UK, mla_bf16 *q_cat, int B,
+                        int S, int H, void *stream);
+
+/* How mla_rope_apply finds the position of row n. */
+typedef enum {
+  MLA_POS_EXPLICIT = 0, /* pos_src = int32 positions [N] */
+  MLA_POS_QUERY = 1,    /* pos_src = seqlens [N / group]; row n = b*group + s sits at
+                           seqlens[b] - group + s (group = S); rows with a negative
+                           position are left untouched */
+  MLA_POS_CACHE = 2     /* pos_src = seqlens [N / group]; row n = b*group + j sits at j
+                           (group = Lmax); rows with j >= seqlens[b] are left untouched */
+} mla_pos_mode;
+
+/*
+ * Rotary position embedding ("YaRN 扩展": the j-th 2-D pair at position m
+ * turns by m * theta_j), on interleaved pairs (x_{2i}, x_{2i+1}) with
+ * theta_i = base^(-2i/64):  (x, y) -> (x cos - y sin, x sin + y cos).
+ * Angles are formed and reduced in fp64, rotated in fp32, stored as bf16.
+ *   x_in  : element (n, i, d) at x_in [n*in_stride_n  + i*in_stride_h  + d], d < 64
+ *   x_out : element (n, i, d) at x_out[n*out_stride_n + i*out_stride_h + d]
+ *           (x_out may equal x_in for an in-place rotation; strides in elements,
+ *            multiples of 8)
+ *   N rows of nh heads each; pos_mode / pos_src / group as in mla_pos_mode.
+ * Queries: x_in = q_rope [B,S,H,64] (strides H*64, 64), x_out = q_cat + 512
+ * (strides H*576, 576), N = B*S, nh = H, MLA_POS_QUERY, group = S.
+ * Cache fill: x_in = x_out = k_R [B,Lmax,64] (strides 64, 0), N = B*Lmax,
+ * nh = 1, MLA_POS_CACHE, group = Lmax.
+ */
+mla_status mla_rope_apply(const mla_bf16 *x_in, int64_t in_stride_n, int64_t in_stride_h,
+                          mla_bf16 *x_out, int64_t out_stride_n, int64_t out_stride_h,
+                          int64_t N, int nh, int pos_mode, const int32_t *pos_src, int group,
+                          float base, void *stream);
+
+/*
+ * Bytes of device workspace mla_decode needs for this shape on the current
+ * device (it depends on the device's SM count).  0 if the shape is
+ * unsupported or no device is present.  The workspace carries the device
+ * status word, the split plan and the fp32 partial results that
+ * mla_splitkv_combine reads.
+ */
+size_t mla_decode_workspace_size(int B, int S, int H);
+
+/*
+ * Latent-space attention of every (b, s, h) query row over its visible
+ * cache rows ("注意力计算" with the absorbed score of "潜在向量的作用"):
+ *   s_j = (q_cat[..,0:512] . c_KV[b,j] + q_cat[..,512:576] . k_R[b,j]) * softmax_scale
+ *   o_lat = sum_j softmax(s)_j c_KV[b,j]      (j = 0 .. L_b - S + s)
+ * The cache rows of a sequence are split over all SMs (split-KV); each split
+ * leaves an fp32 partial result and its log-sum-exp in the workspace, to be
+ * merged by mla_splitkv_combine (call it next, with the same workspace).
+ *   q_cat   [B,S,H,576]  bf16, absorbed + rotated queries
+ *   c_kv    [B,Lmax,512] bf16 latent cache
+ *   k_r     [B,Lmax,64]  bf16 rotated RoPE keys
+ *   seqlens [B] int32 (device), S <= seqlens[b] <= Lmax; rows >= seqlens[b]
+ *           of the cache are never read into a result (they may hold anything)
+ *   softmax_scale: 1/sqrt(192) for the pages' model
+ *   workspace: >= mla_decode_workspace_size(B, S, H) bytes, 256-byte aligned
+ * Requires S in {1, 2}, 1 <= H <= 128.
+ */
+mla_status mla_decode(const mla_bf16 *q_cat, const mla_bf16 *c_kv, const mla_bf16 *k_r,
+                      const int32_t *seqlens, int B, int S, int H, int Lmax, float softmax_scale,
+                      void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Merge the split-KV partials left by mla_decode in `workspace`:
+ *   o_lat = sum_k 2^(lse_k - M) O_k / sum_k 2^(lse_k - M),  M = max_k lse_k
+ * which restores the single normalisation over all visible positions.
+ *   o_lat [B,S,H,512] bf16 output.  B, S, H must match the mla_decode call.
+ */
+mla_status mla_splitkv_combine(const void *workspace, size_t workspace_bytes, mla_bf16 *o_lat,
+                               int B, int S, int H, void *stream);
+
+/*
+ * Up-projection of the latent result ("潜在向量的作用": o = W^UV o_lat),
+ * fp32 accumulation on the tensor cores, rounded to bf16.
+ *   o_lat [B,S,H,512] bf16,  W_UV [H,128,512] bf16 (W_UV[h][v][k]),
+ *   out   [B,S,H,128] bf16 output (per-head output before W^O).
+ */
+mla_status mla_up_project(const mla_bf16 *o_lat, const mla_bf16 *W_UV, mla_bf16 *out, int B,
+                          int S, int H, void *stream);
+
+/*
+ * Synchronise `stream`, return the device-side status recorded in
+ * `workspace` by earlier mla_decode calls (MLA_OK, MLA_ERR_BAD_SEQLEN or
+ * MLA_ERR_TIMEOUT; MLA_ERR_CUDA if the stream reports an error) and clear it.
+ */
+mla_status mla_read_status(void *workspace, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_H */

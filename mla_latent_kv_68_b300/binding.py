@@ -1,0 +1,210 @@
+"""ctypes binding of ``libmla.so`` (the C ABI of include/mla.h).
+
+Argument marshalling only: every function checks tensor dtypes, devices and
+contiguity, passes raw device pointers and the current CUDA stream, and raises
+``MLAError`` for any status other than MLA_OK.  There is no CPU fallback: if
+the CUDA library is missing or no GPU is present, the calls fail.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import re
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmla.so")
+HEADER_PATH = os.path.join(os.path.dirname(_PKG), "include", "mla.h")
+
+MLA_OK = 0
+STATUS_NAMES = {0: "MLA_OK", 1: "MLA_ERR_INVALID_ARG", 2: "MLA_ERR_UNSUPPORTED",
+                3: "MLA_ERR_WORKSPACE", 4: "MLA_ERR_CUDA", 5: "MLA_ERR_BAD_SEQLEN",
+                6: "MLA_ERR_TIMEOUT"}
+POS_EXPLICIT, POS_QUERY, POS_CACHE = 0, 1, 2
+D_C, D_R, D_QK, D_H, D_V = 512, 64, 576, 128, 128
+SOFTMAX_SCALE = 1.0 / math.sqrt(D_H + D_R)
+ROPE_BASE = 10000.0
+
+
+class MLAError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {STATUS_NAMES.get(status, status)}")
+
+
+_lib = None
+
+
+def lib():
+    """Load libmla.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is missing: build it with "
+                              "`python -m mla_latent_kv_68_b300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i32, i64, f32, sz = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float,
+                                 ctypes.c_size_t)
+        L.mla_status_string.restype = ctypes.c_char_p
+        L.mla_status_string.argtypes = [i32]
+        L.mla_version.restype = i32
+        L.mla_absorb_q.argtypes = [vp, vp, vp, i32, i32, i32, vp]
+        L.mla_rope_apply.argtypes = [vp, i64, i64, vp, i64, i64, i64, i32, i32, vp, i32, f32, vp]
+        L.mla_decode_workspace_size.restype = sz
+        L.mla_decode_workspace_size.argtypes = [i32, i32, i32]
+        L.mla_decode.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, f32, vp, sz, vp]
+        L.mla_splitkv_combine.argtypes = [vp, sz, vp, i32, i32, i32, vp]
+        L.mla_up_project.argtypes = [vp, vp, vp, i32, i32, i32, vp]
+        L.mla_read_status.argtypes = [vp, vp]
+        for n in ("mla_absorb_q", "mla_rope_apply", "mla_decode", "mla_splitkv_combine",
+                  "mla_up_project", "mla_read_status"):
+            getattr(L, n).restype = i32
+        _lib = L
+    return _lib
+
+
+def header_symbols() -> list[str]:
+    """Every function the public header declares."""
+    with open(HEADER_PATH) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"\b(mla_[a-z_0-9]+)\s*\(", text)))
+
+
+def _ptr(t: torch.Tensor):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(rc: int, what: str):
+    if rc != MLA_OK:
+        raise MLAError(rc, what)
+
+
+def _need(t: torch.Tensor, name: str, dtype=torch.bfloat16, shape=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def absorb_q(q_nope, W_UK, q_cat, stream=None):
+    """q_cat[..., :512] = W_UK[h]^T q_nope[b,s,h]   (q_nope [B,S,H,128])."""
+    B, S, H, _ = q_nope.shape
+    _need(q_nope, "q_nope", shape=(B, S, H, D_H))
+    _need(W_UK, "W_UK", shape=(H, D_H, D_C))
+    _need(q_cat, "q_cat", shape=(B, S, H, D_QK))
+    _check(lib().mla_absorb_q(_ptr(q_nope), _ptr(W_UK), _ptr(q_cat), B, S, H, _stream(stream)),
+           "mla_absorb_q")
+
+
+def rope_apply(x_in, in_stride_n, in_stride_h, x_out, out_stride_n, out_stride_h, N, nh,
+               pos_mode, pos_src, group=1, base=ROPE_BASE, stream=None):
+    """Raw mla_rope_apply (strides in elements)."""
+    if x_in.dtype != torch.bfloat16 or x_out.dtype != torch.bfloat16:
+        raise TypeError("rope tensors must be bf16")
+    _need(pos_src, "pos_src", dtype=torch.int32)
+    _check(lib().mla_rope_apply(_ptr(x_in), in_stride_n, in_stride_h, _ptr(x_out), out_stride_n,
+                                out_stride_h, N, nh, pos_mode, _ptr(pos_src), group, base,
+                                _stream(stream)), "mla_rope_apply")
+
+
+def rope_queries(q_rope, q_cat, seqlens, base=ROPE_BASE, stream=None):
+    """q_cat[..., 512:] = RoPE(q_rope) at positions seqlens[b] - S + s."""
+    B, S, H, _ = q_rope.shape
+    _need(q_rope, "q_rope", shape=(B, S, H, D_R))
+    _need(q_cat, "q_cat", shape=(B, S, H, D_QK))
+    _need(seqlens, "seqlens", dtype=torch.int32, shape=(B,))
+    out = q_cat.view(-1)[D_C:]
+    rope_apply(q_rope, H * D_R, D_R, out, H * D_QK, D_QK, B * S, H, POS_QUERY, seqlens, S, base,
+               stream)
+
+
+def rope_cache(k_r, seqlens, base=ROPE_BASE, stream=None):
+    """Rotate the cached k_R [B,Lmax,64] in place at positions 0..seqlens[b]-1."""
+    B, Lmax, _ = k_r.shape
+    _need(k_r, "k_r", shape=(B, Lmax, D_R))
+    _need(seqlens, "seqlens", dtype=torch.int32, shape=(B,))
+    rope_apply(k_r, D_R, 0, k_r, D_R, 0, B * Lmax, 1, POS_CACHE, seqlens, Lmax, base, stream)
+
+
+def decode_workspace_size(B: int, S: int, H: int) -> int:
+    n = int(lib().mla_decode_workspace_size(B, S, H))
+    if n == 0:
+        raise MLAError(2, "mla_decode_workspace_size")
+    return n
+
+
+def new_workspace(B: int, S: int, H: int, device=None) -> torch.Tensor:
+    """Zero-filled byte workspace for mla_decode / mla_splitkv_combine."""
+    return torch.zeros(decode_workspace_size(B, S, H), dtype=torch.uint8, device=device or "cuda")
+
+
+def decode(q_cat, c_kv, k_r, seqlens, workspace, softmax_scale=SOFTMAX_SCALE, stream=None):
+    B, S, H, _ = q_cat.shape
+    Lmax = c_kv.shape[1]
+    _need(q_cat, "q_cat", shape=(B, S, H, D_QK))
+    _need(c_kv, "c_kv", shape=(B, Lmax, D_C))
+    _need(k_r, "k_r", shape=(B, Lmax, D_R))
+    _need(seqlens, "seqlens", dtype=torch.int32, shape=(B,))
+    _need(workspace, "workspace", dtype=torch.uint8)
+    _check(lib().mla_decode(_ptr(q_cat), _ptr(c_kv), _ptr(k_r), _ptr(seqlens), B, S, H, Lmax,
+                            softmax_scale, _ptr(workspace), workspace.numel(), _stream(stream)),
+           "mla_decode")
+
+
+def splitkv_combine(workspace, o_lat, stream=None):
+    B, S, H, _ = o_lat.shape
+    _need(o_lat, "o_lat", shape=(B, S, H, D_C))
+    _need(workspace, "workspace", dtype=torch.uint8)
+    _check(lib().mla_splitkv_combine(_ptr(workspace), workspace.numel(), _ptr(o_lat), B, S, H,
+                                     _stream(stream)), "mla_splitkv_combine")
+
+
+def up_project(o_lat, W_UV, out, stream=None):
+    B, S, H, _ = o_lat.shape
+    _need(o_lat, "o_lat", shape=(B, S, H, D_C))
+    _need(W_UV, "W_UV", shape=(H, D_V, D_C))
+    _need(out, "out", shape=(B, S, H, D_V))
+    _check(lib().mla_up_project(_ptr(o_lat), _ptr(W_UV), _ptr(out), B, S, H, _stream(stream)),
+           "mla_up_project")
+
+
+def read_status(workspace=None, stream=None) -> int:
+    """Synchronise and return (and clear) the device-side status."""
+    ws = _ptr(workspace) if workspace is not None else ctypes.c_void_p(0)
+    return int(lib().mla_read_status(ws, _stream(stream)))
+
+
+class DecodeStep:
+    """Owns the per-step device buffers of one decode shape and issues the
+    five library calls of a step on one stream:
+    absorb -> RoPE(queries) -> decode -> combine -> up-project."""
+
+    def __init__(self, B: int, S: int, H: int, device="cuda"):
+        self.B, self.S, self.H = B, S, H
+        self.q_cat = torch.empty(B, S, H, D_QK, dtype=torch.bfloat16, device=device)
+        self.o_lat = torch.empty(B, S, H, D_C, dtype=torch.bfloat16, device=device)
+        self.out = torch.empty(B, S, H, D_V, dtype=torch.bfloat16, device=device)
+        self.workspace = new_workspace(B, S, H, device)
+
+    def __call__(self, q_nope, q_rope, c_kv, k_r, seqlens, W_UK, W_UV,
+                 softmax_scale=SOFTMAX_SCALE, stream=None):
+        absorb_q(q_nope, W_UK, self.q_cat, stream)
+        rope_queries(q_rope, self.q_cat, seqlens, stream=stream)
+        decode(self.q_cat, c_kv, k_r, seqlens, self.workspace, softmax_scale, stream)
+        splitkv_combine(self.workspace, self.o_lat, stream)
+        up_project(self.o_lat, W_UV, self.out, stream)
+        return self.out
+
+    LAUNCHES_PER_STEP = 6  # absorb, rope, plan, decode, combine, up-projection

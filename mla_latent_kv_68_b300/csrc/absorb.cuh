@@ -1,0 +1,118 @@
+// absorb.cuh -- q~ = (W^UK_h)^T q^C per head, on the tcgen05 tensor cores.
+//
+// "DeepSeek-V3" (ekkoxiao.github.io), "Multi-Head Latent Attention /
+// 潜在向量的作用": (q^C)^T W^UK c = ((W^UK)^T q^C)^T c, so the key
+// up-projection moves onto the query once per decode step.
+//
+// Per head h this is [B*S x 128] x [128 x 512].  B*S is small (1..256), so
+// the weight goes in the MMA's M slot: the kernel computes
+//     D[k, n] = sum_d W_UK[h][d][k] * q_nope[n][h][d]      (M = k, N = n, K = d)
+// with A = W_UK[h] read as an MN-major operand (k is contiguous in memory)
+// and B = the q^C rows as a K-major operand.  One CTA owns one head, one
+// 128-wide block of k and one tile of up to 256 query rows; fp32 accumulates
+// in tensor memory and the epilogue rounds to bf16 into q_cat[n][h][k].
+//
+// Shared memory (128-byte swizzle, 1024-byte aligned):
+//   A: 2 atoms x [128 d][64 k] bf16            32 KB
+//   B: 2 atoms x [n_tile rows][64 d] bf16      n_tile * 256 B
+#pragma once
+
+#include "sm100.cuh"
+
+namespace mla {
+
+constexpr int kAbsorbThreads = 128;
+
+struct AbsorbParams {
+  __nv_bfloat16* q_cat;  // [BS, H, 576]
+  int BS, H, n_tile;     // n_tile: multiple of 16, <= 256
+  uint32_t tmem_cols;    // power of two >= max(32, n_tile)
+  uint32_t* status;
+  uint64_t timeout_ns;
+};
+
+__global__ void __launch_bounds__(kAbsorbThreads, 1)
+    absorb_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_q,
+                  const AbsorbParams p) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int h = blockIdx.x;
+  const int mb = blockIdx.y;               // 128-wide block of the latent index k
+  const int n0 = blockIdx.z * p.n_tile;    // first query row of this tile
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + 32768;
+  const uint32_t abytes = (uint32_t)p.n_tile * 128u;  // one 64-wide d atom of B
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + 2 * abytes);  // [0] full, [1] mma done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2);
+  volatile uint32_t* abort_flag = tmem_slot + 1;
+  WaitCtx wc{abort_flag, p.status, p.timeout_ns};
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    mbar_init(&bars[0], 1);
+    mbar_init(&bars[1], 1);
+    fence_mbar_init_cluster();
+    tma_prefetch_desc(&tm_w);
+    tma_prefetch_desc(&tm_q);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, p.tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (threadIdx.x == 0) {
+    mbar_arrive_expect_tx(&bars[0], 32768u + 2 * abytes);
+    for (int a = 0; a < 2; ++a) {
+      tma_load_3d(sA + a * 16384, &tm_w, &bars[0], mb * 128 + a * 64, 0, h);
+      tma_load_3d(sB + a * abytes, &tm_q, &bars[0], a * 64, h, n0);
+    }
+    if (mbar_wait(&bars[0], 0, wc)) {
+      tc_fence_after();
+      const uint32_t idesc = idesc_bf16_f32(128, p.n_tile, /*a_mn=*/1, /*b_mn=*/0);
+      const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {  // K = 128 in steps of 16
+        // A, MN-major: 16 d-rows per step (2048 B); the two 64-wide k atoms sit 16 KB apart.
+        const uint64_t ad = smem_desc(a0 + kk * 2048, 16384, 1024, 2);
+        // B, K-major: step kk lies in atom kk/4 at a 32-byte offset inside the 128-byte row.
+        const uint64_t bd = smem_desc(b0 + (kk >> 2) * abytes + (kk & 3) * 32, 16, 1024, 2);
+        mma_ss(tmem, ad, bd, idesc, kk > 0 ? 1u : 0u);
+      }
+      mma_commit(&bars[1]);
+    }
+  }
+  __syncwarp();
+
+  const bool ok = mbar_wait(&bars[1], 0, wc);
+  tc_fence_after();
+  if (ok) {
+    const int k = mb * 128 + warp * 32 + lane;  // this thread's tensor-memory lane
+    const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
+    const int nvalid = min(p.n_tile, p.BS - n0);
+    for (int c0 = 0; c0 < p.n_tile; c0 += 16) {
+      uint32_t r[16];
+      tmem_ld16(tl + c0, r);
+      tmem_wait_ld();
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const int n = n0 + c0 + c;
+        if (c0 + c < nvalid)
+          p.q_cat[((size_t)n * p.H + h) * 576 + k] = __float2bfloat16_rn(__uint_as_float(r[c]));
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, p.tmem_cols);
+  }
+}
+
+}  // namespace mla

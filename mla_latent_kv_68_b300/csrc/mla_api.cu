@@ -1,0 +1,382 @@
+// mla_api.cu -- the C ABI declared in include/mla.h: argument validation,
+// TMA tensor-map encoding, per-device launch configuration and the launches.
+// No call allocates device memory or synchronises (except mla_read_status).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "mla.h"
+
+#include "absorb.cuh"
+#include "decode.cuh"
+#include "rope.cuh"
+#include "splitkv.cuh"
+#include "up_project.cuh"
+
+namespace {
+
+// Status word of the kernels that take no workspace (absorb, up-projection).
+__device__ uint32_t g_kernel_status;
+
+constexpr uint64_t kTimeoutNs = 1000000000ull;  // bounded waits give up after 1 s
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  bool ready = false;
+  int num_sms = 0;
+  int max_clusters = 0;       // co-resident 2-CTA decode clusters
+  uint32_t* kernel_status = nullptr;
+};
+
+std::mutex g_mutex;
+DeviceInfo g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Per-device set-up: kernel attributes, decode cluster occupancy, status symbol.
+const DeviceInfo* device_info() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceInfo& d = g_dev[dev];
+  if (d.ready) return &d;
+  if (!g_encode) {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr)
+      return nullptr;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return nullptr;
+  if (cudaFuncSetAttribute(mla::decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           mla::kDecSmem) != cudaSuccess ||
+      cudaFuncSetAttribute(mla::decode_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 0) !=
+          cudaSuccess ||
+      cudaFuncSetAttribute(mla::absorb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           32768 + 65536 + 64) != cudaSuccess ||
+      cudaFuncSetAttribute(mla::up_project_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           8 * 16384 + 8 * 64 * 128 + 128) != cudaSuccess)
+    return nullptr;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(2 * d.num_sms);
+  cfg.blockDim = dim3(mla::kDecThreads);
+  cfg.dynamicSmemBytes = mla::kDecSmem;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&clusters, mla::decode_kernel, &cfg) != cudaSuccess ||
+      clusters < 1)
+    return nullptr;
+  d.max_clusters = clusters;
+  void* sym = nullptr;
+  if (cudaGetSymbolAddress(&sym, g_kernel_status) != cudaSuccess) return nullptr;
+  d.kernel_status = static_cast<uint32_t*>(sym);
+  d.ready = true;
+  return &d;
+}
+
+bool encode_tiled(CUtensorMap* map, const void* base, cuuint32_t rank, const cuuint64_t* dims,
+                  const cuuint64_t* strides_bytes, const cuuint32_t* box) {
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims,
+                  strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Workspace layout of mla_decode / mla_splitkv_combine.
+struct WsLayout {
+  int n_rb = 0, G = 0, slots = 0;
+  size_t prefix = 0, gfirst = 0, segbase = 0, ml = 0, opart = 0, total = 0;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+WsLayout ws_layout(int B, int S, int H, int max_clusters) {
+  WsLayout w;
+  w.n_rb = (S * H + 127) / 128;
+  w.G = max_clusters / w.n_rb;
+  if (w.G < 1) w.G = 1;
+  w.slots = w.G + B;  // every group boundary inside a sequence adds one segment
+  size_t off = 256;   // [0] sticky device status, [1] plan_ok
+  w.prefix = off;  off = align256(off + sizeof(int32_t) * (B + 1));
+  w.gfirst = off;  off = align256(off + sizeof(int32_t) * B);
+  w.segbase = off; off = align256(off + sizeof(int32_t) * (B + 1));
+  w.ml = off;      off = align256(off + sizeof(float) * 2 * (size_t)w.slots * w.n_rb * 128);
+  w.opart = off;   off = align256(off + sizeof(float) * (size_t)w.slots * w.n_rb * 128 * 512);
+  w.total = off;
+  return w;
+}
+
+bool decode_shape_ok(int B, int S, int H) {
+  return B >= 1 && S >= 1 && H >= 1 && H <= 128 && S * H <= 2048 && B <= (1 << 20);
+}
+
+mla_status launch_status() {
+  return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+uint32_t pow2_at_least(uint32_t x) {
+  uint32_t p = 32;
+  while (p < x) p <<= 1;
+  return p;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* mla_status_string(int s) {
+  switch (s) {
+    case MLA_OK: return "MLA_OK";
+    case MLA_ERR_INVALID_ARG: return "MLA_ERR_INVALID_ARG";
+    case MLA_ERR_UNSUPPORTED: return "MLA_ERR_UNSUPPORTED";
+    case MLA_ERR_WORKSPACE: return "MLA_ERR_WORKSPACE";
+    case MLA_ERR_CUDA: return "MLA_ERR_CUDA";
+    case MLA_ERR_BAD_SEQLEN: return "MLA_ERR_BAD_SEQLEN";
+    case MLA_ERR_TIMEOUT: return "MLA_ERR_TIMEOUT";
+    default: return "MLA_ERR_UNKNOWN";
+  }
+}
+
+int mla_version(void) { return 100; }
+
+mla_status mla_absorb_q(const mla_bf16* q_nope, const mla_bf16* W_UK, mla_bf16* q_cat, int B,
+                        int S, int H, void* stream) {
+  if (!q_nope || !W_UK || !q_cat || !aligned16(q_nope) || !aligned16(W_UK) || !aligned16(q_cat))
+    return MLA_ERR_INVALID_ARG;
+  if (B < 1 || S < 1 || H < 1) return MLA_ERR_INVALID_ARG;
+  if (H > 128) return MLA_ERR_UNSUPPORTED;
+  const long long BS = (long long)B * S;
+  if (BS > 65535LL * 256) return MLA_ERR_UNSUPPORTED;
+  const DeviceInfo* dev = device_info();
+  if (!dev) return MLA_ERR_CUDA;
+  const int n_tile = BS >= 256 ? 256 : (int)((BS + 15) / 16 * 16);
+  CUtensorMap tw, tq;
+  const cuuint64_t wd[3] = {512, 128, (cuuint64_t)H};
+  const cuuint64_t ws[2] = {1024, 128 * 1024};
+  const cuuint32_t wb[3] = {64, 128, 1};
+  const cuuint64_t qd[3] = {128, (cuuint64_t)H, (cuuint64_t)BS};
+  const cuuint64_t qs[2] = {256, (cuuint64_t)H * 256};
+  const cuuint32_t qb[3] = {64, 1, (cuuint32_t)n_tile};
+  if (!encode_tiled(&tw, W_UK, 3, wd, ws, wb) || !encode_tiled(&tq, q_nope, 3, qd, qs, qb))
+    return MLA_ERR_INVALID_ARG;
+  mla::AbsorbParams p;
+  p.q_cat = reinterpret_cast<__nv_bfloat16*>(q_cat);
+  p.BS = (int)BS;
+  p.H = H;
+  p.n_tile = n_tile;
+  p.tmem_cols = pow2_at_least((uint32_t)n_tile);
+  p.status = dev->kernel_status;
+  p.timeout_ns = kTimeoutNs;
+  const dim3 grid(H, 4, (unsigned)((BS + n_tile - 1) / n_tile));
+  const size_t smem = 32768 + (size_t)n_tile * 256 + 64;
+  mla::absorb_kernel<<<grid, mla::kAbsorbThreads, smem, (cudaStream_t)stream>>>(tw, tq, p);
+  return launch_status();
+}
+
+mla_status mla_rope_apply(const mla_bf16* x_in, int64_t in_stride_n, int64_t in_stride_h,
+                          mla_bf16* x_out, int64_t out_stride_n, int64_t out_stride_h, int64_t N,
+                          int nh, int pos_mode, const int32_t* pos_src, int group, float base,
+                          void* stream) {
+  if (!x_in || !x_out || !pos_src || !aligned16(x_in) || !aligned16(x_out)) return MLA_ERR_INVALID_ARG;
+  if (N < 0 || nh < 1 || !(base > 1.0f) || !std::isfinite(base)) return MLA_ERR_INVALID_ARG;
+  if ((in_stride_n | in_stride_h | out_stride_n | out_stride_h) & 7) return MLA_ERR_INVALID_ARG;
+  if (in_stride_n < 0 || in_stride_h < 0 || out_stride_n < 0 || out_stride_h < 0)
+    return MLA_ERR_INVALID_ARG;
+  if (pos_mode != mla::kPosExplicit && pos_mode != mla::kPosQuery && pos_mode != mla::kPosCache)
+    return MLA_ERR_INVALID_ARG;
+  if (pos_mode != mla::kPosExplicit && group < 1) return MLA_ERR_INVALID_ARG;
+  if (N == 0) return MLA_OK;
+  mla::RopeTheta th;
+  for (int j = 0; j < 32; ++j) th.theta[j] = std::pow((double)base, -2.0 * j / 64.0);
+  const long long threads = N * (long long)nh * 8;
+  const int block = 256;
+  const long long grid = (threads + block - 1) / block;
+  if (grid > 0x7fffffffLL) return MLA_ERR_UNSUPPORTED;
+  mla::rope_kernel<<<(unsigned)grid, block, 0, (cudaStream_t)stream>>>(
+      reinterpret_cast<const __nv_bfloat16*>(x_in), in_stride_n, in_stride_h,
+      reinterpret_cast<__nv_bfloat16*>(x_out), out_stride_n, out_stride_h, N, nh, pos_mode,
+      pos_src, group, th);
+  return launch_status();
+}
+
+size_t mla_decode_workspace_size(int B, int S, int H) {
+  if (!decode_shape_ok(B, S, H)) return 0;
+  const DeviceInfo* dev = device_info();
+  if (!dev) return 0;
+  return ws_layout(B, S, H, dev->max_clusters).total;
+}
+
+mla_status mla_decode(const mla_bf16* q_cat, const mla_bf16* c_kv, const mla_bf16* k_r,
+                      const int32_t* seqlens, int B, int S, int H, int Lmax, float softmax_scale,
+                      void* workspace, size_t workspace_bytes, void* stream) {
+  if (!q_cat || !c_kv || !k_r || !seqlens || !aligned16(q_cat) || !aligned16(c_kv) ||
+      !aligned16(k_r))
+    return MLA_ERR_INVALID_ARG;
+  if (B < 1 || S < 1 || H < 1 || Lmax < 1 || !(softmax_scale > 0.f) || !std::isfinite(softmax_scale))
+    return MLA_ERR_INVALID_ARG;
+  if (!decode_shape_ok(B, S, H)) return MLA_ERR_UNSUPPORTED;
+  if ((long long)B * Lmax + 64 > 0x7fffffffLL) return MLA_ERR_UNSUPPORTED;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return MLA_ERR_WORKSPACE;
+  const DeviceInfo* dev = device_info();
+  if (!dev) return MLA_ERR_CUDA;
+  const WsLayout w = ws_layout(B, S, H, dev->max_clusters);
+  if (workspace_bytes < w.total) return MLA_ERR_WORKSPACE;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  cudaStream_t st = (cudaStream_t)stream;
+
+  mla::PlanParams pp;
+  pp.seqlens = seqlens;
+  pp.B = B;
+  pp.S = S;
+  pp.Lmax = Lmax;
+  pp.G = w.G;
+  pp.prefix = reinterpret_cast<int32_t*>(ws + w.prefix);
+  pp.gfirst = reinterpret_cast<int32_t*>(ws + w.gfirst);
+  pp.segbase = reinterpret_cast<int32_t*>(ws + w.segbase);
+  pp.status = reinterpret_cast<uint32_t*>(ws);
+  pp.plan_ok = reinterpret_cast<uint32_t*>(ws) + 1;
+  mla::plan_kernel<<<1, 1024, 0, st>>>(pp);
+  if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
+
+  CUtensorMap tc, tk;
+  const cuuint64_t cd[2] = {512, (cuuint64_t)B * Lmax};
+  const cuuint64_t cs[1] = {1024};
+  const cuuint32_t cb[2] = {64, 64};
+  const cuuint64_t kd[2] = {64, (cuuint64_t)B * Lmax};
+  const cuuint64_t ks[1] = {128};
+  if (!encode_tiled(&tc, c_kv, 2, cd, cs, cb) || !encode_tiled(&tk, k_r, 2, kd, ks, cb))
+    return MLA_ERR_INVALID_ARG;
+
+  mla::DecodeParams p;
+  p.q_cat = reinterpret_cast<const __nv_bfloat16*>(q_cat);
+  p.seqlens = seqlens;
+  p.prefix = pp.prefix;
+  p.gfirst = pp.gfirst;
+  p.segbase = pp.segbase;
+  p.ml = reinterpret_cast<float2*>(ws + w.ml);
+  p.opart = reinterpret_cast<float*>(ws + w.opart);
+  p.status = pp.status;
+  p.plan_ok = pp.plan_ok;
+  p.B = B;
+  p.S = S;
+  p.H = H;
+  p.Lmax = Lmax;
+  p.n_rb = w.n_rb;
+  p.G = w.G;
+  p.scale_log2 = softmax_scale * 1.4426950408889634f;
+  p.timeout_ns = kTimeoutNs;
+
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(2 * w.G * w.n_rb);
+  cfg.blockDim = dim3(mla::kDecThreads);
+  cfg.dynamicSmemBytes = mla::kDecSmem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, mla::decode_kernel, tc, tk, p) != cudaSuccess) return MLA_ERR_CUDA;
+  return launch_status();
+}
+
+mla_status mla_splitkv_combine(const void* workspace, size_t workspace_bytes, mla_bf16* o_lat,
+                               int B, int S, int H, void* stream) {
+  if (!o_lat || !aligned16(o_lat)) return MLA_ERR_INVALID_ARG;
+  if (B < 1 || S < 1 || H < 1) return MLA_ERR_INVALID_ARG;
+  if (!decode_shape_ok(B, S, H)) return MLA_ERR_UNSUPPORTED;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return MLA_ERR_WORKSPACE;
+  const DeviceInfo* dev = device_info();
+  if (!dev) return MLA_ERR_CUDA;
+  const WsLayout w = ws_layout(B, S, H, dev->max_clusters);
+  if (workspace_bytes < w.total) return MLA_ERR_WORKSPACE;
+  const uint8_t* ws = static_cast<const uint8_t*>(workspace);
+  mla::CombineParams p;
+  p.segbase = reinterpret_cast<const int32_t*>(ws + w.segbase);
+  p.ml = reinterpret_cast<const float2*>(ws + w.ml);
+  p.opart = reinterpret_cast<const float*>(ws + w.opart);
+  p.o_lat = reinterpret_cast<__nv_bfloat16*>(o_lat);
+  p.plan_ok = reinterpret_cast<const uint32_t*>(ws) + 1;
+  p.B = B;
+  p.S = S;
+  p.H = H;
+  p.n_rb = w.n_rb;
+  const long long rows = (long long)B * S * H;
+  const unsigned grid = (unsigned)((rows + 7) / 8);
+  mla::combine_kernel<<<grid, 256, 0, (cudaStream_t)stream>>>(p);
+  return launch_status();
+}
+
+mla_status mla_up_project(const mla_bf16* o_lat, const mla_bf16* W_UV, mla_bf16* out, int B,
+                          int S, int H, void* stream) {
+  if (!o_lat || !W_UV || !out || !aligned16(o_lat) || !aligned16(W_UV) || !aligned16(out))
+    return MLA_ERR_INVALID_ARG;
+  if (B < 1 || S < 1 || H < 1) return MLA_ERR_INVALID_ARG;
+  if (H > 128) return MLA_ERR_UNSUPPORTED;
+  const long long BS = (long long)B * S;
+  if (BS > 65535LL * 64) return MLA_ERR_UNSUPPORTED;
+  const DeviceInfo* dev = device_info();
+  if (!dev) return MLA_ERR_CUDA;
+  const int n_tile = BS >= 64 ? 64 : (int)((BS + 15) / 16 * 16);
+  CUtensorMap tw, to;
+  const cuuint64_t wd[3] = {512, 128, (cuuint64_t)H};
+  const cuuint64_t ws[2] = {1024, 128 * 1024};
+  const cuuint32_t wb[3] = {64, 128, 1};
+  const cuuint64_t od[3] = {512, (cuuint64_t)H, (cuuint64_t)BS};
+  const cuuint64_t os[2] = {1024, (cuuint64_t)H * 1024};
+  const cuuint32_t ob[3] = {64, 1, (cuuint32_t)n_tile};
+  if (!encode_tiled(&tw, W_UV, 3, wd, ws, wb) || !encode_tiled(&to, o_lat, 3, od, os, ob))
+    return MLA_ERR_INVALID_ARG;
+  mla::UpParams p;
+  p.out = reinterpret_cast<__nv_bfloat16*>(out);
+  p.BS = (int)BS;
+  p.H = H;
+  p.n_tile = n_tile;
+  p.tmem_cols = pow2_at_least((uint32_t)n_tile);
+  p.status = dev->kernel_status;
+  p.timeout_ns = kTimeoutNs;
+  const dim3 grid(H, (unsigned)((BS + n_tile - 1) / n_tile));
+  const size_t smem = 8 * 16384 + (size_t)8 * n_tile * 128 + 128;
+  mla::up_project_kernel<<<grid, mla::kUpThreads, smem, (cudaStream_t)stream>>>(tw, to, p);
+  return launch_status();
+}
+
+mla_status mla_read_status(void* workspace, void* stream) {
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MLA_ERR_CUDA;
+  const DeviceInfo* dev = device_info();
+  if (!dev) return MLA_ERR_CUDA;
+  uint32_t bits = 0, kbits = 0;
+  if (workspace) {
+    if (cudaMemcpy(&bits, workspace, sizeof bits, cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemset(workspace, 0, sizeof bits) != cudaSuccess)
+      return MLA_ERR_CUDA;
+  }
+  if (cudaMemcpy(&kbits, dev->kernel_status, sizeof kbits, cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemset(dev->kernel_status, 0, sizeof kbits) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  bits |= kbits;
+  if (bits & mla::kDevErrInternal) return MLA_ERR_CUDA;
+  if (bits & mla::kDevErrTimeout) return MLA_ERR_TIMEOUT;
+  if (bits & mla::kDevErrBadSeqlen) return MLA_ERR_BAD_SEQLEN;
+  return MLA_OK;
+}
+
+}  // extern "C"

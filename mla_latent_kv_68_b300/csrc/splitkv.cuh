@@ -1,0 +1,173 @@
+// splitkv.cuh -- split-KV plan and log-sum-exp combine.
+//
+// The softmax of "DeepSeek-V3" (ekkoxiao.github.io), "Multi-Head Latent
+// Attention / 注意力计算" normalises once over all visible positions.  The
+// decode kernel cuts every sequence's cache rows into contiguous runs of
+// 64-row tiles ("segments") spread over all SMs; each segment k leaves, per
+// query row, an unnormalised latent sum O_k = sum_j 2^(s2_j - m_k) c_j, its
+// reference exponent m_k (an integer, log2 units) and l_k = sum_j 2^(s2_j - m_k).
+// Merging them restores the single normalisation exactly:
+//     o_lat = sum_k 2^(m_k - M) O_k / sum_k 2^(m_k - M) l_k,   M = max_k m_k.
+//
+// Plan: the cache tiles of all sequences are laid end to end (sequence-major)
+// and cut into G equal runs, one per group of clusters.  Group g owns flat
+// tiles [floor(g T / G), floor((g+1) T / G)).  A sequence b contributes one
+// segment to every group its tiles touch; its segments get consecutive slot
+// numbers starting at segbase[b].
+#pragma once
+
+#include "sm100.cuh"
+
+namespace mla {
+
+struct PlanParams {
+  const int32_t* seqlens;
+  int B, S, Lmax, G;
+  int32_t* prefix;   // [B+1] exclusive prefix of tiles per sequence; prefix[B] = T
+  int32_t* gfirst;   // [B] first group touching sequence b
+  int32_t* segbase;  // [B+1] exclusive prefix of segments per sequence
+  uint32_t* status;
+  uint32_t* plan_ok;
+};
+
+__device__ __forceinline__ int tiles_of(int L) { return (L + 63) >> 6; }
+
+// Group owning flat tile x: the largest g with floor(g T / G) <= x.
+__device__ __forceinline__ int group_of(int64_t x, int64_t T, int G) {
+  return (int)(((x + 1) * G - 1) / T);
+}
+
+// Block-wide exclusive scan of one int per thread (blockDim.x a multiple of 32).
+__device__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int inc = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += t;
+  }
+  if (lane == 31) warp_sums[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < nw ? warp_sums[lane] : 0;
+    int winc = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, winc, o);
+      if (lane >= o) winc += t;
+    }
+    if (lane < nw) warp_sums[lane] = winc - w;
+    if (lane == nw - 1) warp_sums[32] = winc;
+  }
+  __syncthreads();
+  const int excl = warp_sums[warp] + inc - v;
+  *total = warp_sums[32];
+  __syncthreads();
+  return excl;
+}
+
+__global__ void __launch_bounds__(1024) plan_kernel(const PlanParams p) {
+  __shared__ int warp_sums[33];
+  __shared__ int bad;
+  const int nt = blockDim.x;
+  if (threadIdx.x == 0) bad = 0;
+  __syncthreads();
+  const int E = (p.B + nt - 1) / nt;
+  const int beg = min(p.B, (int)threadIdx.x * E), end = min(p.B, beg + E);
+
+  int local = 0;
+  for (int b = beg; b < end; ++b) {
+    const int L = p.seqlens[b];
+    if (L < p.S || L > p.Lmax) bad = 1;
+    else local += tiles_of(L);
+  }
+  int T;
+  int run = block_exclusive_scan(local, warp_sums, &T);
+  for (int b = beg; b < end; ++b) {
+    p.prefix[b] = run;
+    const int L = p.seqlens[b];
+    if (L >= p.S && L <= p.Lmax) run += tiles_of(L);
+  }
+  if (threadIdx.x == 0) p.prefix[p.B] = T;
+  __syncthreads();
+
+  local = 0;
+  for (int b = beg; b < end; ++b) {
+    const int x0 = p.prefix[b], x1 = p.prefix[b + 1];
+    int ns = 0, gf = 0;
+    if (x1 > x0) {
+      gf = group_of(x0, T, p.G);
+      ns = group_of(x1 - 1, T, p.G) - gf + 1;
+    }
+    p.gfirst[b] = gf;
+    local += ns;
+  }
+  int nseg_total;
+  run = block_exclusive_scan(local, warp_sums, &nseg_total);
+  for (int b = beg; b < end; ++b) {
+    p.segbase[b] = run;
+    const int x0 = p.prefix[b], x1 = p.prefix[b + 1];
+    if (x1 > x0) run += group_of(x1 - 1, T, p.G) - group_of(x0, T, p.G) + 1;
+  }
+  if (threadIdx.x == 0) {
+    p.segbase[p.B] = nseg_total;
+    *p.plan_ok = bad ? 0u : 1u;
+    if (bad) atomicOr(p.status, kDevErrBadSeqlen);
+  }
+}
+
+struct CombineParams {
+  const int32_t* segbase;
+  const float2* ml;     // [slots * n_rb * 128] (m_k, l_k)
+  const float* opart;   // [slots * n_rb * 128, 512]
+  __nv_bfloat16* o_lat; // [B*S*H, 512]
+  const uint32_t* plan_ok;
+  int B, S, H, n_rb;
+};
+
+// One warp per (b, s, h) row; each lane owns 16 consecutive latent columns.
+__global__ void __launch_bounds__(256) combine_kernel(const CombineParams p) {
+  const int row = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  const int SH = p.S * p.H;
+  if (row >= p.B * SH) return;
+  if (*p.plan_ok == 0u) return;
+  const int b = row / SH, gr = row - b * SH;
+  const int rb = gr >> 7, r = gr & 127;
+  const int k0 = p.segbase[b], k1 = p.segbase[b + 1];
+
+  float M = -INFINITY;
+  for (int k = k0; k < k1; ++k) {
+    const float2 v = p.ml[((size_t)k * p.n_rb + rb) * 128 + r];
+    if (v.y > 0.f) M = fmaxf(M, v.x);
+  }
+  float acc[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+  float den = 0.f;
+  for (int k = k0; k < k1; ++k) {
+    const size_t idx = ((size_t)k * p.n_rb + rb) * 128 + r;
+    const float2 v = p.ml[idx];
+    if (!(v.y > 0.f)) continue;
+    const float w = exp2f(v.x - M);
+    den += w * v.y;
+    const float4* src = reinterpret_cast<const float4*>(p.opart + idx * 512 + lane * 16);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float4 o = src[q];
+      acc[4 * q + 0] += w * o.x;
+      acc[4 * q + 1] += w * o.y;
+      acc[4 * q + 2] += w * o.z;
+      acc[4 * q + 3] += w * o.w;
+    }
+  }
+  const float inv = den > 0.f ? 1.f / den : 0.f;
+  uint32_t packed[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) packed[i] = pack_bf16x2(acc[2 * i] * inv, acc[2 * i + 1] * inv);
+  uint4* dst = reinterpret_cast<uint4*>(p.o_lat + (size_t)row * 512 + lane * 16);
+  dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+  dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+}
+
+}  // namespace mla

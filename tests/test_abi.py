@@ -1,0 +1,55 @@
+"""The C-ABI library loads and exports every symbol the header declares, and
+host-side validation rejects bad arguments before any launch (no GPU needed)."""
+import ctypes
+import shutil
+
+import pytest
+
+from mla_latent_kv_68_b300 import binding, build
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if shutil.which("nvcc") or __import__("os").path.exists("/usr/local/cuda/bin/nvcc"):
+        build.build()
+    return binding.lib()
+
+
+def test_header_declares_the_five_steps():
+    syms = binding.header_symbols()
+    for name in ("mla_absorb_q", "mla_rope_apply", "mla_decode", "mla_splitkv_combine",
+                 "mla_up_project"):
+        assert name in syms
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in binding.header_symbols():
+        assert hasattr(lib, name), f"{name} not exported by libmla.so"
+
+
+def test_status_strings_and_version(lib):
+    for code, name in binding.STATUS_NAMES.items():
+        assert lib.mla_status_string(code).decode() == name
+    assert lib.mla_status_string(99).decode() == "MLA_ERR_UNKNOWN"
+    assert lib.mla_version() >= 100
+
+
+def test_null_pointers_rejected_on_host(lib):
+    nul = ctypes.c_void_p(0)
+    assert lib.mla_absorb_q(nul, nul, nul, 1, 1, 1, nul) == 1
+    assert lib.mla_up_project(nul, nul, nul, 1, 1, 1, nul) == 1
+    assert lib.mla_decode(nul, nul, nul, nul, 1, 1, 1, 1, 0.1, nul, 0, nul) == 1
+    assert lib.mla_splitkv_combine(nul, 0, nul, 1, 1, 1, nul) == 1
+    assert lib.mla_rope_apply(nul, 64, 0, nul, 64, 0, 1, 1, 0, nul, 1, 10000.0, nul) == 1
+
+
+def test_bad_sizes_rejected_on_host(lib):
+    fake = ctypes.c_void_p(1 << 20)  # aligned, never dereferenced: validation fails first
+    assert lib.mla_absorb_q(fake, fake, fake, 0, 1, 1, None) == 1
+    assert lib.mla_absorb_q(fake, fake, fake, 1, 1, 129, None) == 2
+    assert lib.mla_up_project(fake, fake, fake, 1, 1, 200, None) == 2
+    assert lib.mla_rope_apply(fake, 63, 0, fake, 64, 0, 1, 1, 0, fake, 1, 10000.0, None) == 1
+    assert lib.mla_rope_apply(fake, 64, 0, fake, 64, 0, 1, 1, 7, fake, 1, 10000.0, None) == 1
+    assert lib.mla_decode(fake, fake, fake, fake, 1, 1, 1, 1, -1.0, fake, 0, None) == 1
+    misaligned = ctypes.c_void_p((1 << 20) + 8)
+    assert lib.mla_absorb_q(misaligned, fake, fake, 1, 1, 1, None) == 1
