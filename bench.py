@@ -198,52 +198,63 @@ def run_ours(args, x, rank, world, local_rank):
     if mb.read_status(step.workspace) != mb.MLA_OK:
         raise RuntimeError("device status not clean after warm-up")
 
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
-    _barrier(world)
-    torch.cuda.synchronize(dev)
-    with ClockSampler(local_rank) as clocks:
-        for i in range(args.steps):
-            flush.zero_()
-            e = ev[i]
-            e[0].record(stream)
-            mb.absorb_q(d["q_nope"], d["W_UK"], step.q_cat)
-            mb.rope_queries(d["q_rope"], step.q_cat, d["seqlens"])
-            e[1].record(stream)
-            mb.decode(step.q_cat, d["c_kv"], d["k_r"], d["seqlens"], step.workspace)
-            e[2].record(stream)
-            mb.splitkv_combine(step.workspace, step.o_lat)
-            mb.up_project(step.o_lat, d["W_UV"], step.out)
-            e[3].record(stream)
+    # CUDA graphs of the library calls: the whole step, and its three phases
+    g_all = step.capture(step, *args_step)
+    g_q = step.capture(step.queries, d["q_nope"], d["q_rope"], d["seqlens"], d["W_UK"])
+    g_a = step.capture(step.attend, d["c_kv"], d["k_r"], d["seqlens"])
+    g_p = step.capture(step.project, d["W_UV"])
+    for _ in range(args.warmup):
+        g_all.replay()
+
+    def timed(body, n_events):
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n_events)]
+              for _ in range(args.steps)]
+        _barrier(world)
         torch.cuda.synchronize(dev)
-    _barrier(world)
+        for i in range(args.steps):
+            flush.zero_()          # L2 flush between steps; the host runs ahead meanwhile
+            body(ev[i])
+        torch.cuda.synchronize(dev)
+        _barrier(world)
+        return ev
+
+    with ClockSampler(local_rank) as clocks:
+        ev_all = timed(lambda e: (e[0].record(stream), g_all.replay(), e[1].record(stream)), 2)
+        ev_ph = timed(lambda e: (e[0].record(stream), g_q.replay(), e[1].record(stream),
+                                 g_a.replay(), e[2].record(stream), g_p.replay(),
+                                 e[3].record(stream)), 4)
     if mb.read_status(step.workspace) != mb.MLA_OK:
         raise RuntimeError("device status not clean after the timed steps")
-    step_ms = [e[0].elapsed_time(e[3]) for e in ev]
-    dec_ms = [e[1].elapsed_time(e[2]) for e in ev]
-    step_us = _max_over_ranks(statistics.mean(step_ms) * 1000, world)
-    dec_us = _max_over_ranks(statistics.mean(dec_ms) * 1000, world)
+    step_us = _max_over_ranks(statistics.mean(e[0].elapsed_time(e[1]) for e in ev_all) * 1000, world)
+    q_us = _max_over_ranks(statistics.mean(e[0].elapsed_time(e[1]) for e in ev_ph) * 1000, world)
+    dec_us = _max_over_ranks(statistics.mean(e[1].elapsed_time(e[2]) for e in ev_ph) * 1000, world)
+    p_us = _max_over_ranks(statistics.mean(e[2].elapsed_time(e[3]) for e in ev_ph) * 1000, world)
 
-    # end to end through the C ABI from pinned host buffers (query in, output back)
+    # end to end through the public API from pinned host buffers: the query is
+    # copied in, the step's graph replays, the output is copied back
     hq = x["q_nope"].pin_memory()
     hr = x["q_rope"].pin_memory()
     hl = x["seqlens"].pin_memory()
     hout = torch.empty(step.out.shape, dtype=torch.bfloat16).pin_memory()
-    q_dev, r_dev, l_dev = torch.empty_like(d["q_nope"]), torch.empty_like(d["q_rope"]), torch.empty_like(d["seqlens"])
     h2d = hq.numel() * 2 + hr.numel() * 2 + hl.numel() * 4
     d2h = hout.numel() * 2
-    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(args.steps)]
-    for i in range(args.steps):
-        flush.zero_()
-        e2e_ev[i][0].record(stream)
-        q_dev.copy_(hq, non_blocking=True)
-        r_dev.copy_(hr, non_blocking=True)
-        l_dev.copy_(hl, non_blocking=True)
-        step(q_dev, r_dev, d["c_kv"], d["k_r"], l_dev, d["W_UK"], d["W_UV"])
+
+    def e2e_body(e, replay=True):
+        e[0].record(stream)
+        d["q_nope"].copy_(hq, non_blocking=True)
+        d["q_rope"].copy_(hr, non_blocking=True)
+        d["seqlens"].copy_(hl, non_blocking=True)
+        if replay:
+            g_all.replay()
+        else:
+            step(*args_step)
         hout.copy_(step.out, non_blocking=True)
-        e2e_ev[i][1].record(stream)
-    torch.cuda.synchronize(dev)
-    e2e_us = _max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in e2e_ev) * 1000, world)
+        e[1].record(stream)
+
+    ev_e2e = timed(e2e_body, 2)
+    e2e_us = _max_over_ranks(statistics.mean(e[0].elapsed_time(e[1]) for e in ev_e2e) * 1000, world)
+    ev_eager = timed(lambda e: e2e_body(e, replay=False), 2)
+    eager_us = _max_over_ranks(statistics.mean(e[0].elapsed_time(e[1]) for e in ev_eager) * 1000, world)
 
     if rank != 0:
         return
@@ -262,13 +273,15 @@ def run_ours(args, x, rank, world, local_rank):
                      "peak_source": src,
                      "tensor_tflops": round(wk["dec_flops"] / (dec_us * 1e-6) / 1e12, 1),
                      "tensor_frac_of_burst": round(wk["dec_flops"] / (dec_us * 1e-6) / 1e12 / tf_burst, 4)},
-        "kernels": {"decode_us": round(dec_us, 3), "step_us": round(step_us, 3),
+        "kernels": {"queries_us": round(q_us, 3), "decode_us": round(dec_us, 3),
+                    "combine_project_us": round(p_us, 3), "step_us": round(step_us, 3),
                     "step_roofline_us": round(max(wk["step_bytes"] / (hbm * 1e3),
                                                   wk["step_flops"] / (tf_burst * 1e6)), 3),
                     "algorithmic_decode_bytes": wk["dec_bytes"],
                     "algorithmic_decode_flops": wk["dec_flops"]},
         "e2e": {"value": round(e2e_us, 3), "unit": "us/step", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h, "path": "pinned host -> H2D -> step graph -> D2H",
+                "eager_calls_value": round(eager_us, 3)},
         "gpu_launches": mb.DecodeStep.LAUNCHES_PER_STEP * args.steps,
         "clocks": clocks.summary(),
     }

@@ -200,11 +200,32 @@ class DecodeStep:
 
     def __call__(self, q_nope, q_rope, c_kv, k_r, seqlens, W_UK, W_UV,
                  softmax_scale=SOFTMAX_SCALE, stream=None):
+        self.queries(q_nope, q_rope, seqlens, W_UK, stream)
+        self.attend(c_kv, k_r, seqlens, softmax_scale, stream)
+        self.project(W_UV, stream)
+        return self.out
+
+    # The three phases of a step, separately callable for per-phase timing.
+    def queries(self, q_nope, q_rope, seqlens, W_UK, stream=None):
         absorb_q(q_nope, W_UK, self.q_cat, stream)
         rope_queries(q_rope, self.q_cat, seqlens, stream=stream)
+
+    def attend(self, c_kv, k_r, seqlens, softmax_scale=SOFTMAX_SCALE, stream=None):
         decode(self.q_cat, c_kv, k_r, seqlens, self.workspace, softmax_scale, stream)
+
+    def project(self, W_UV, stream=None):
         splitkv_combine(self.workspace, self.o_lat, stream)
         up_project(self.o_lat, W_UV, self.out, stream)
-        return self.out
+
+    def capture(self, fn, *args, **kwargs):
+        """Record ``fn(*args)`` (library calls only) into a CUDA graph and
+        return it; ``graph.replay()`` re-issues the same launches on the
+        current stream with no host work per kernel.  The graph reads the
+        same device buffers on every replay, so new query or length values
+        copied into them take effect."""
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn(*args, **kwargs)
+        return g
 
     LAUNCHES_PER_STEP = 6  # absorb, rope, plan, decode, combine, up-projection

@@ -17,9 +17,10 @@
 //   rank 0 ("score CTA"): Q lives in its tensor memory (288 columns) and is
 //       the A operand of the QK^T MMAs (A-from-TMEM form); two 64-column S
 //       buffers; it streams full 576-wide cache rows through a 3-stage TMA
-//       ring, runs the online softmax and writes P (bf16, already in the
-//       128-byte-swizzled MMA layout) and the per-row rescale factor straight
-//       into rank 1's shared memory (distributed shared memory).
+//       ring, runs the online softmax and sends P (bf16, already in the
+//       128-byte-swizzled MMA layout) and the per-row rescale factor into
+//       rank 1's shared memory with asynchronous remote stores (st.async)
+//       whose bytes complete a transaction-counted barrier there.
 //   rank 1 ("value CTA"): O lives in all 512 columns of its tensor memory; it
 //       streams the 512-wide c rows of the same tiles (they are L2 hits right
 //       after rank 0's reads) and issues O += P . C with C read as an
@@ -59,6 +60,7 @@ constexpr int kPBytes = 128 * kTok * 2;
 constexpr int kOffAlpha = kOffP + 2 * kPBytes;      // value CTA: alpha[2][128] f32
 constexpr int kOffBar = kOffAlpha + 2 * 128 * 4;
 constexpr int kNumBars = 21;
+constexpr uint32_t kPTx = kPBytes + 128 * 4;  // bytes of one P slot + its alpha column
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kDecSmem = kOffMisc + 16;
 static_assert(kStages * kStage0 <= kOffBar, "score CTA stages overlap the barriers");
@@ -84,8 +86,9 @@ struct DecodeParams {
   const int32_t* prefix;       // plan (splitkv.cuh)
   const int32_t* gfirst;
   const int32_t* segbase;
-  float2* ml;                  // [slots * n_rb * 128]
-  float* opart;                // [slots * n_rb * 128, 512]
+  const int32_t* gstart;       // [G] first sequence of each group's run
+  float2* ml;                  // [slots * n_rb, 128]        (m, l) per row
+  float* opart;                // [slots * n_rb, 512, 128]   column-major O per segment
   uint32_t* status;
   const uint32_t* plan_ok;
   int B, S, H, Lmax, n_rb, G;
@@ -105,14 +108,8 @@ __device__ __forceinline__ void for_each_tile(const DecodeParams& p, int g, F&& 
   if (T <= 0) return;
   const int64_t beg = (int64_t)g * T / p.G, end = (int64_t)(g + 1) * T / p.G;
   if (beg >= end) return;
-  int lo = 0, hi = p.B - 1;  // largest b with prefix[b] <= beg
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (p.prefix[mid] <= beg) lo = mid;
-    else hi = mid - 1;
-  }
   int i = 0, k = 0;
-  for (int b = lo; b < p.B; ++b) {
+  for (int b = p.gstart[g]; b < p.B; ++b) {
     const int64_t x0 = p.prefix[b], x1 = p.prefix[b + 1];
     if (x0 >= end) break;
     if (x1 <= beg) continue;
@@ -165,13 +162,17 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       mbar_init(&bar[B_SFULL + s], 1);
       mbar_init(&bar[B_SEMPTY + s], 128);
       mbar_init(&bar[B_PEMPTY + s], 1);
-      mbar_init(&bar[B_PFULL + s], 128);
+      mbar_init(&bar[B_PFULL + s], 1);
       mbar_init(&bar[B_PREADY + s], 128);
       mbar_init(&bar[B_PVDONE + s], 1);
     }
     mbar_init(&bar[B_QREADY], 128);
     mbar_init(&bar[B_OFREE], 128);
     mbar_init(&bar[B_DRAIN], 1);
+    if (rank == 1) {  // first phase of each P slot expects one slot's bytes
+      mbar_arrive_expect_tx(&bar[B_PFULL + 0], kPTx);
+      mbar_arrive_expect_tx(&bar[B_PFULL + 1], kPTx);
+    }
     fence_mbar_init_cluster();
     tma_prefetch_desc(&tm_c);
     tma_prefetch_desc(&tm_kr);
@@ -240,6 +241,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
           if (!mbar_wait(&bar[B_PREADY + slot], sph, wc)) return false;
           if (ti.first && ti.k > 0 && !mbar_wait(&bar[B_OFREE], (uint32_t)(ti.k - 1) & 1u, wc))
             return false;
+          fence_proxy_async_cta();  // P arrived through the generic proxy; the MMA reads it
           tc_fence_after();
           const int nvt = min(ti.L - ti.t * kTok, kTok);
           const int nk = (nvt + 15) >> 4;
@@ -285,6 +287,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       // ---------------------------------------- scores + online softmax
       const uint32_t p_remote = map_to_cta(smem_u32(smem + kOffP), 1);
       const uint32_t a_remote = map_to_cta(smem_u32(smem + kOffAlpha), 1);
+      const uint32_t pfull_remote = map_to_cta(smem_u32(&bar[B_PFULL]), 1);
       float m_ref = -INFINITY, l = 0.f;
       int limit = 0;
       for_each_tile(p, g, [&](const TileInfo& ti) {
@@ -293,14 +296,17 @@ __global__ void __launch_bounds__(kDecThreads, 1)
           const uint4* qrow = reinterpret_cast<const uint4*>(
               p.q_cat + (((size_t)ti.b * p.S + s_r) * p.H + h_r) * 576);
 #pragma unroll 1
-          for (int c = 0; c < 9; ++c) {
-            uint32_t v[32];
+          for (int c3 = 0; c3 < 9; c3 += 3) {  // 3 x 3 chunks: 24 loads in flight per thread
+            uint32_t v[3][32];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              const uint4 x = valid ? __ldg(qrow + c * 8 + u) : make_uint4(0, 0, 0, 0);
-              v[4 * u] = x.x; v[4 * u + 1] = x.y; v[4 * u + 2] = x.z; v[4 * u + 3] = x.w;
-            }
-            tmem_st32(tl + kQCol + (uint32_t)c * 32, v);
+            for (int c = 0; c < 3; ++c)
+#pragma unroll
+              for (int u = 0; u < 8; ++u) {
+                const uint4 x = valid ? __ldg(qrow + (c3 + c) * 8 + u) : make_uint4(0, 0, 0, 0);
+                v[c][4 * u] = x.x; v[c][4 * u + 1] = x.y; v[c][4 * u + 2] = x.z; v[c][4 * u + 3] = x.w;
+              }
+#pragma unroll
+            for (int c = 0; c < 3; ++c) tmem_st32(tl + kQCol + (uint32_t)(c3 + c) * 32, v[c]);
           }
           tmem_wait_st();
           tc_fence_before();
@@ -353,13 +359,12 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 
         if (!warp_wait(&bar[B_PEMPTY + slot], sph ^ 1u, wc)) return false;
         const uint32_t row = p_remote + (uint32_t)slot * kPBytes + (uint32_t)r * 128;
+        const uint32_t rbar = pfull_remote + (uint32_t)slot * 8;
 #pragma unroll
         for (int ch = 0; ch < 8; ++ch)  // 128-byte swizzle: chunk ch of row r sits at ch ^ (r & 7)
-          st_cluster_v4(row + (uint32_t)((ch ^ (r & 7)) << 4),
-                        make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]));
-        st_cluster_f32(a_remote + (uint32_t)(slot * 128 + r) * 4, alpha);
-        fence_proxy_async_cluster();
-        mbar_arrive_remote(&bar[B_PFULL + slot], 1);
+          st_async_v4(row + (uint32_t)((ch ^ (r & 7)) << 4),
+                      make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]), rbar);
+        st_async_f32(a_remote + (uint32_t)(slot * 128 + r) * 4, alpha, rbar);
         if (ti.last && valid) p.ml[((size_t)ti.slot * p.n_rb + rb) * 128 + r] = make_float2(mu, l);
         return true;
       });
@@ -372,6 +377,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         const uint32_t sph = (uint32_t)(ti.i >> 1) & 1u, ph = (uint32_t)(ti.i / kStages) & 1u;
         if (!warp_wait(&bar[B_PFULL + slot], sph, wc)) return false;
         const float alpha = alpha_buf[slot * 128 + r];
+        if (wt == 0) mbar_arrive_expect_tx(&bar[B_PFULL + slot], kPTx);  // arm the slot's next phase
         const bool need = !ti.first && alpha != 1.f;
         if (__any_sync(0xffffffffu, need)) {
           // O rows change only after the previous tile's P . C has completed
@@ -409,8 +415,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         if (ti.last) {
           if (!warp_wait(&bar[B_PVDONE + slot], sph, wc)) return false;
           tc_fence_after();
-          float4* dst = reinterpret_cast<float4*>(
-              p.opart + (((size_t)ti.slot * p.n_rb + rb) * 128 + r) * 512);
+          // column-major [512][128]: for each column a warp stores 32 consecutive floats
+          float* dst = p.opart + ((size_t)ti.slot * p.n_rb + rb) * 512 * 128 + r;
 #pragma unroll 1
           for (int c = 0; c < 16; ++c) {
             uint32_t v[32];
@@ -418,9 +424,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             tmem_wait_ld();
             if (valid) {
 #pragma unroll
-              for (int u = 0; u < 8; ++u)
-                dst[c * 8 + u] = make_float4(__uint_as_float(v[4 * u]), __uint_as_float(v[4 * u + 1]),
-                                             __uint_as_float(v[4 * u + 2]), __uint_as_float(v[4 * u + 3]));
+              for (int u = 0; u < 32; ++u) dst[(size_t)(c * 32 + u) * 128] = __uint_as_float(v[u]);
             }
           }
           tc_fence_before();

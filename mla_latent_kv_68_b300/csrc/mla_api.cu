@@ -100,7 +100,7 @@ bool encode_tiled(CUtensorMap* map, const void* base, cuuint32_t rank, const cuu
 // Workspace layout of mla_decode / mla_splitkv_combine.
 struct WsLayout {
   int n_rb = 0, G = 0, slots = 0;
-  size_t prefix = 0, gfirst = 0, segbase = 0, ml = 0, opart = 0, total = 0;
+  size_t prefix = 0, gfirst = 0, segbase = 0, gstart = 0, ml = 0, opart = 0, total = 0;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -115,6 +115,7 @@ WsLayout ws_layout(int B, int S, int H, int max_clusters) {
   w.prefix = off;  off = align256(off + sizeof(int32_t) * (B + 1));
   w.gfirst = off;  off = align256(off + sizeof(int32_t) * B);
   w.segbase = off; off = align256(off + sizeof(int32_t) * (B + 1));
+  w.gstart = off;  off = align256(off + sizeof(int32_t) * w.G);
   w.ml = off;      off = align256(off + sizeof(float) * 2 * (size_t)w.slots * w.n_rb * 128);
   w.opart = off;   off = align256(off + sizeof(float) * (size_t)w.slots * w.n_rb * 128 * 512);
   w.total = off;
@@ -248,6 +249,7 @@ mla_status mla_decode(const mla_bf16* q_cat, const mla_bf16* c_kv, const mla_bf1
   pp.prefix = reinterpret_cast<int32_t*>(ws + w.prefix);
   pp.gfirst = reinterpret_cast<int32_t*>(ws + w.gfirst);
   pp.segbase = reinterpret_cast<int32_t*>(ws + w.segbase);
+  pp.gstart = reinterpret_cast<int32_t*>(ws + w.gstart);
   pp.status = reinterpret_cast<uint32_t*>(ws);
   pp.plan_ok = reinterpret_cast<uint32_t*>(ws) + 1;
   mla::plan_kernel<<<1, 1024, 0, st>>>(pp);
@@ -268,6 +270,7 @@ mla_status mla_decode(const mla_bf16* q_cat, const mla_bf16* c_kv, const mla_bf1
   p.prefix = pp.prefix;
   p.gfirst = pp.gfirst;
   p.segbase = pp.segbase;
+  p.gstart = pp.gstart;
   p.ml = reinterpret_cast<float2*>(ws + w.ml);
   p.opart = reinterpret_cast<float*>(ws + w.opart);
   p.status = pp.status;
@@ -318,9 +321,8 @@ mla_status mla_splitkv_combine(const void* workspace, size_t workspace_bytes, ml
   p.S = S;
   p.H = H;
   p.n_rb = w.n_rb;
-  const long long rows = (long long)B * S * H;
-  const unsigned grid = (unsigned)((rows + 7) / 8);
-  mla::combine_kernel<<<grid, 256, 0, (cudaStream_t)stream>>>(p);
+  const dim3 grid((unsigned)(B * w.n_rb), 8);
+  mla::combine_kernel<<<grid, 128, 0, (cudaStream_t)stream>>>(p);
   return launch_status();
 }
 

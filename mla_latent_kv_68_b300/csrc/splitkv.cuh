@@ -26,6 +26,7 @@ struct PlanParams {
   int32_t* prefix;   // [B+1] exclusive prefix of tiles per sequence; prefix[B] = T
   int32_t* gfirst;   // [B] first group touching sequence b
   int32_t* segbase;  // [B+1] exclusive prefix of segments per sequence
+  int32_t* gstart;   // [G] first sequence touched by each group
   uint32_t* status;
   uint32_t* plan_ok;
 };
@@ -109,6 +110,16 @@ __global__ void __launch_bounds__(1024) plan_kernel(const PlanParams p) {
     const int x0 = p.prefix[b], x1 = p.prefix[b + 1];
     if (x1 > x0) run += group_of(x1 - 1, T, p.G) - group_of(x0, T, p.G) + 1;
   }
+  for (int g = threadIdx.x; g < p.G; g += nt) {  // largest b with prefix[b] <= floor(g T / G)
+    const int64_t tg = (int64_t)g * T / p.G;
+    int lo = 0, hi = p.B - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (p.prefix[mid] <= tg) lo = mid;
+      else hi = mid - 1;
+    }
+    p.gstart[g] = lo;
+  }
   if (threadIdx.x == 0) {
     p.segbase[p.B] = nseg_total;
     *p.plan_ok = bad ? 0u : 1u;
@@ -118,22 +129,23 @@ __global__ void __launch_bounds__(1024) plan_kernel(const PlanParams p) {
 
 struct CombineParams {
   const int32_t* segbase;
-  const float2* ml;     // [slots * n_rb * 128] (m_k, l_k)
-  const float* opart;   // [slots * n_rb * 128, 512]
+  const float2* ml;     // [slots * n_rb, 128] (m_k, l_k)
+  const float* opart;   // [slots * n_rb, 512, 128] column-major
   __nv_bfloat16* o_lat; // [B*S*H, 512]
   const uint32_t* plan_ok;
   int B, S, H, n_rb;
 };
 
-// One warp per (b, s, h) row; each lane owns 16 consecutive latent columns.
-__global__ void __launch_bounds__(256) combine_kernel(const CombineParams p) {
-  const int row = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
-  const int lane = threadIdx.x & 31;
+// Block = one 128-row block of one sequence and 64 latent columns; thread =
+// one query row.  Partials are column-major, so every load of a warp reads 32
+// consecutive floats.
+__global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
+  const int b = blockIdx.x / p.n_rb, rb = blockIdx.x - b * p.n_rb;
+  const int c0 = blockIdx.y * 64;
+  const int r = threadIdx.x;
   const int SH = p.S * p.H;
-  if (row >= p.B * SH) return;
+  if (rb * 128 + r >= SH) return;
   if (*p.plan_ok == 0u) return;
-  const int b = row / SH, gr = row - b * SH;
-  const int rb = gr >> 7, r = gr & 127;
   const int k0 = p.segbase[b], k1 = p.segbase[b + 1];
 
   float M = -INFINITY;
@@ -141,33 +153,28 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineParams p) {
     const float2 v = p.ml[((size_t)k * p.n_rb + rb) * 128 + r];
     if (v.y > 0.f) M = fmaxf(M, v.x);
   }
-  float acc[16];
+  float acc[64];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+  for (int i = 0; i < 64; ++i) acc[i] = 0.f;
   float den = 0.f;
   for (int k = k0; k < k1; ++k) {
-    const size_t idx = ((size_t)k * p.n_rb + rb) * 128 + r;
-    const float2 v = p.ml[idx];
+    const size_t idx = (size_t)k * p.n_rb + rb;
+    const float2 v = p.ml[idx * 128 + r];
     if (!(v.y > 0.f)) continue;
     const float w = exp2f(v.x - M);
     den += w * v.y;
-    const float4* src = reinterpret_cast<const float4*>(p.opart + idx * 512 + lane * 16);
+    const float* src = p.opart + (idx * 512 + c0) * 128 + r;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const float4 o = src[q];
-      acc[4 * q + 0] += w * o.x;
-      acc[4 * q + 1] += w * o.y;
-      acc[4 * q + 2] += w * o.z;
-      acc[4 * q + 3] += w * o.w;
-    }
+    for (int c = 0; c < 64; ++c) acc[c] += w * __ldg(src + (size_t)c * 128);
   }
   const float inv = den > 0.f ? 1.f / den : 0.f;
-  uint32_t packed[8];
+  uint4* dst = reinterpret_cast<uint4*>(p.o_lat + ((size_t)b * SH + rb * 128 + r) * 512 + c0);
 #pragma unroll
-  for (int i = 0; i < 8; ++i) packed[i] = pack_bf16x2(acc[2 * i] * inv, acc[2 * i + 1] * inv);
-  uint4* dst = reinterpret_cast<uint4*>(p.o_lat + (size_t)row * 512 + lane * 16);
-  dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-  dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+  for (int q = 0; q < 8; ++q)
+    dst[q] = make_uint4(pack_bf16x2(acc[8 * q] * inv, acc[8 * q + 1] * inv),
+                        pack_bf16x2(acc[8 * q + 2] * inv, acc[8 * q + 3] * inv),
+                        pack_bf16x2(acc[8 * q + 4] * inv, acc[8 * q + 5] * inv),
+                        pack_bf16x2(acc[8 * q + 6] * inv, acc[8 * q + 7] * inv));
 }
 
 }  // namespace mla
