@@ -162,6 +162,36 @@ mla_status mla_up_project(const mla_bf16 *o_lat, const mla_bf16 *W_UV, mla_bf16 
  */
 mla_status mla_read_status(void *workspace, void *stream);
 
+/*
+ * Allocation-free latent decode: mla_decode followed by mla_splitkv_combine,
+ * with the split-KV workspace taken from a fixed scratch array inside the
+ * library instead of from the caller.  The paper has no counterpart; this
+ * entry exists for callers that cannot allocate device memory on their
+ * decode path -- a serving process that reserves all of HBM for its own pool
+ * up front, or a real-time loop that must not call cudaMalloc because it can
+ * synchronise the device and stall other streams.
+ *   q_cat, c_kv, k_r, seqlens, B, S, H, Lmax, softmax_scale: as mla_decode
+ *   o_lat [B,S,H,512] bf16 output, as mla_splitkv_combine
+ * Scratch: one MLA_STATIC_SCRATCH_BYTES array per device, reserved when the
+ * library's device code is loaded on that device and held until the process
+ * exits.  A shape is accepted when mla_decode_workspace_size(B, S, H) is at
+ * most MLA_STATIC_SCRATCH_BYTES (32 MiB: e.g. B = 32, S = 1, H = 128 on a
+ * 148-SM B300); a larger one returns MLA_ERR_WORKSPACE and launches nothing.
+ * Every call on a device shares that one array and leaves its contents
+ * behind; each call writes every scratch byte it reads before reading it, so
+ * nothing has to be cleared between calls.  Calls whose kernels overlap on
+ * the GPU (different streams, no ordering between them) race on the array
+ * and give wrong results: order them on one stream.
+ * The first call on a device looks up the array's device address (with that
+ * device current); make that first call before any stream capture.
+ * Device-side errors go to the library status word, read by
+ * mla_read_status(NULL, stream).  The call allocates and frees nothing.
+ */
+enum { MLA_STATIC_SCRATCH_BYTES = 32 << 20 };
+mla_status mla_decode_noalloc(const mla_bf16 *q_cat, const mla_bf16 *c_kv, const mla_bf16 *k_r,
+                              const int32_t *seqlens, int B, int S, int H, int Lmax,
+                              float softmax_scale, mla_bf16 *o_lat, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -25,6 +25,7 @@ STATUS_NAMES = {0: "MLA_OK", 1: "MLA_ERR_INVALID_ARG", 2: "MLA_ERR_UNSUPPORTED",
 POS_EXPLICIT, POS_QUERY, POS_CACHE = 0, 1, 2
 D_C, D_R, D_QK, D_H, D_V = 512, 64, 576, 128, 128
 SOFTMAX_SCALE = 1.0 / math.sqrt(D_H + D_R)
+STATIC_SCRATCH_BYTES = 32 << 20   # MLA_STATIC_SCRATCH_BYTES of include/mla.h
 ROPE_BASE = 10000.0
 
 
@@ -58,8 +59,9 @@ def lib():
         L.mla_splitkv_combine.argtypes = [vp, sz, vp, i32, i32, i32, vp]
         L.mla_up_project.argtypes = [vp, vp, vp, i32, i32, i32, vp]
         L.mla_read_status.argtypes = [vp, vp]
+        L.mla_decode_noalloc.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, f32, vp, vp]
         for n in ("mla_absorb_q", "mla_rope_apply", "mla_decode", "mla_splitkv_combine",
-                  "mla_up_project", "mla_read_status"):
+                  "mla_up_project", "mla_read_status", "mla_decode_noalloc"):
             getattr(L, n).restype = i32
         _lib = L
     return _lib
@@ -178,6 +180,23 @@ def up_project(o_lat, W_UV, out, stream=None):
     _need(out, "out", shape=(B, S, H, D_V))
     _check(lib().mla_up_project(_ptr(o_lat), _ptr(W_UV), _ptr(out), B, S, H, _stream(stream)),
            "mla_up_project")
+
+
+def decode_noalloc(q_cat, c_kv, k_r, seqlens, o_lat, softmax_scale=SOFTMAX_SCALE, stream=None):
+    """mla_decode + mla_splitkv_combine with the library's own fixed scratch
+    array instead of a caller workspace, for callers that cannot allocate
+    device memory on their decode path.  Device errors are read with
+    ``read_status()`` (no workspace argument)."""
+    B, S, H, _ = q_cat.shape
+    Lmax = c_kv.shape[1]
+    _need(q_cat, "q_cat", shape=(B, S, H, D_QK))
+    _need(c_kv, "c_kv", shape=(B, Lmax, D_C))
+    _need(k_r, "k_r", shape=(B, Lmax, D_R))
+    _need(seqlens, "seqlens", dtype=torch.int32, shape=(B,))
+    _need(o_lat, "o_lat", shape=(B, S, H, D_C))
+    _check(lib().mla_decode_noalloc(_ptr(q_cat), _ptr(c_kv), _ptr(k_r), _ptr(seqlens), B, S, H,
+                                    Lmax, softmax_scale, _ptr(o_lat), _stream(stream)),
+           "mla_decode_noalloc")
 
 
 def read_status(workspace=None, stream=None) -> int:

@@ -382,3 +382,127 @@ mla_status mla_read_status(void* workspace, void* stream) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free decode (mla_decode_noalloc).  For callers that cannot
+// allocate device memory on their decode path, the split-KV workspace lives
+// in this fixed array instead of a caller buffer.  In host code the name
+// g_static_scratch is only a host-side stand-in for the symbol; the device
+// address comes from cudaGetSymbolAddress, looked up once per device.
+namespace {
+
+__device__ __align__(256) uint8_t g_static_scratch[MLA_STATIC_SCRATCH_BYTES];
+
+std::mutex g_static_mutex;
+uint8_t* g_static_addr[kMaxDevices] = {};
+
+// Device address of g_static_scratch on the current device (nullptr on error).
+uint8_t* static_scratch() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_static_mutex);
+  if (!g_static_addr[dev]) {
+    void* addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_static_scratch) != cudaSuccess || addr == nullptr)
+      return nullptr;
+    g_static_addr[dev] = static_cast<uint8_t*>(addr);
+  }
+  return g_static_addr[dev];
+}
+
+}  // namespace
+
+extern "C" mla_status mla_decode_noalloc(const mla_bf16* q_cat, const mla_bf16* c_kv,
+                                         const mla_bf16* k_r, const int32_t* seqlens, int B,
+                                         int S, int H, int Lmax, float softmax_scale,
+                                         mla_bf16* o_lat, void* stream) {
+  if (!q_cat || !c_kv || !k_r || !seqlens || !o_lat || !aligned16(q_cat) || !aligned16(c_kv) ||
+      !aligned16(k_r) || !aligned16(o_lat))
+    return MLA_ERR_INVALID_ARG;
+  if (B < 1 || S < 1 || H < 1 || Lmax < 1 || !(softmax_scale > 0.f) || !std::isfinite(softmax_scale))
+    return MLA_ERR_INVALID_ARG;
+  if (!decode_shape_ok(B, S, H)) return MLA_ERR_UNSUPPORTED;
+  if ((long long)B * Lmax + 64 > 0x7fffffffLL) return MLA_ERR_UNSUPPORTED;
+  const DeviceInfo* dev = device_info();
+  if (!dev) return MLA_ERR_CUDA;
+  const WsLayout w = ws_layout(B, S, H, dev->max_clusters);
+  if (w.total > (size_t)MLA_STATIC_SCRATCH_BYTES) return MLA_ERR_WORKSPACE;
+  uint8_t* ws = static_scratch();
+  if (!ws) return MLA_ERR_CUDA;
+  cudaStream_t st = (cudaStream_t)stream;
+  // Device errors go to the library status word; word [1] of the scratch is
+  // the plan's ok flag, rewritten by the plan kernel on every call.
+  uint32_t* status = dev->kernel_status;
+  uint32_t* plan_ok = reinterpret_cast<uint32_t*>(ws) + 1;
+
+  mla::PlanParams pp;
+  pp.seqlens = seqlens;
+  pp.B = B;
+  pp.S = S;
+  pp.Lmax = Lmax;
+  pp.G = w.G;
+  pp.prefix = reinterpret_cast<int32_t*>(ws + w.prefix);
+  pp.gfirst = reinterpret_cast<int32_t*>(ws + w.gfirst);
+  pp.segbase = reinterpret_cast<int32_t*>(ws + w.segbase);
+  pp.gstart = reinterpret_cast<int32_t*>(ws + w.gstart);
+  pp.status = status;
+  pp.plan_ok = plan_ok;
+  mla::plan_kernel<<<1, 1024, 0, st>>>(pp);
+  if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
+
+  CUtensorMap tc, tk;
+  const cuuint64_t cd[2] = {512, (cuuint64_t)B * Lmax};
+  const cuuint64_t cs[1] = {1024};
+  const cuuint32_t cb[2] = {64, 64};
+  const cuuint64_t kd[2] = {64, (cuuint64_t)B * Lmax};
+  const cuuint64_t ks[1] = {128};
+  if (!encode_tiled(&tc, c_kv, 2, cd, cs, cb) || !encode_tiled(&tk, k_r, 2, kd, ks, cb))
+    return MLA_ERR_INVALID_ARG;
+
+  mla::DecodeParams p;
+  p.q_cat = reinterpret_cast<const __nv_bfloat16*>(q_cat);
+  p.seqlens = seqlens;
+  p.prefix = pp.prefix;
+  p.gfirst = pp.gfirst;
+  p.segbase = pp.segbase;
+  p.gstart = pp.gstart;
+  p.ml = reinterpret_cast<float2*>(ws + w.ml);
+  p.opart = reinterpret_cast<float*>(ws + w.opart);
+  p.status = status;
+  p.plan_ok = plan_ok;
+  p.B = B;
+  p.S = S;
+  p.H = H;
+  p.Lmax = Lmax;
+  p.n_rb = w.n_rb;
+  p.G = w.G;
+  p.scale_log2 = softmax_scale * 1.4426950408889634f;
+  p.timeout_ns = kTimeoutNs;
+
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(2 * w.G * w.n_rb);
+  cfg.blockDim = dim3(mla::kDecThreads);
+  cfg.dynamicSmemBytes = mla::kDecSmem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, mla::decode_kernel, tc, tk, p) != cudaSuccess) return MLA_ERR_CUDA;
+
+  mla::CombineParams cp;
+  cp.segbase = pp.segbase;
+  cp.ml = p.ml;
+  cp.opart = p.opart;
+  cp.o_lat = reinterpret_cast<__nv_bfloat16*>(o_lat);
+  cp.plan_ok = plan_ok;
+  cp.B = B;
+  cp.S = S;
+  cp.H = H;
+  cp.n_rb = w.n_rb;
+  mla::combine_kernel<<<dim3((unsigned)(B * w.n_rb), 8), 128, 0, st>>>(cp);
+  return launch_status();
+}

@@ -53,3 +53,10 @@ def test_bad_sizes_rejected_on_host(lib):
     assert lib.mla_decode(fake, fake, fake, fake, 1, 1, 1, 1, -1.0, fake, 0, None) == 1
     misaligned = ctypes.c_void_p((1 << 20) + 8)
     assert lib.mla_absorb_q(misaligned, fake, fake, 1, 1, 1, None) == 1
+
+
+def test_static_scratch_limit_matches_the_header():
+    import re
+    with open(binding.HEADER_PATH) as f:
+        m = re.search(r"MLA_STATIC_SCRATCH_BYTES\s*=\s*(\d+)\s*<<\s*(\d+)", f.read())
+    assert m and int(m.group(1)) << int(m.group(2)) == binding.STATIC_SCRATCH_BYTES
