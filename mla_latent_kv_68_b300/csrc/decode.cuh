@@ -6,27 +6,36 @@
 //   softmax over the visible positions, aggregation in latent space
 //           o_lat = sum_j a_j c_j                                   ("潜在向量的作用")
 // All query rows of one sequence (S*H of them, up to 128 per "row block")
-// share every cache tile, so one tile feeds two dense contractions:
-//   S[128 x 64]   = Q[128 x 576] . K_tile[64 x 576]^T      (K = [c ; k^R])
-//   O[128 x 512] += P[128 x 64]  . C_tile[64 x 512]
+// share every cache tile, so one 128-token tile feeds two dense contractions:
+//   S[128 x 128]   = Q[128 x 576] . K_tile[128 x 576]^T      (K = [c ; k^R])
+//   O[128 x 512]  += P[128 x 128] . C_tile[128 x 512]
 //
-// B300 mapping.  The fp32 accumulator O (128 x 512) fills one SM's entire
-// tensor memory, and Q (128 x 576 bf16) plus a cache tile do not fit one SM's
-// shared memory next to it.  So each unit of work runs on a CLUSTER OF TWO
-// CTAs on two SMs:
-//   rank 0 ("score CTA"): Q lives in its tensor memory (288 columns) and is
-//       the A operand of the QK^T MMAs (A-from-TMEM form); two 64-column S
-//       buffers; it streams full 576-wide cache rows through a 3-stage TMA
-//       ring, runs the online softmax and sends P (bf16, already in the
-//       128-byte-swizzled MMA layout) and the per-row rescale factor into
-//       rank 1's shared memory with asynchronous remote stores (st.async)
-//       whose bytes complete a transaction-counted barrier there.
+// B300 mapping.  A tcgen05 MMA of M = 128 runs at the full tensor rate only
+// from N = 128 up (N = 64 reaches about half of it), so both contractions use
+// N >= 128.  The fp32 accumulator O (128 x 512) fills one SM's whole tensor
+// memory, so each unit of work is a CLUSTER OF TWO CTAs on two SMs:
+//   rank 0 ("score CTA"): q~ (128 x 512 bf16) lives in its tensor memory as
+//       the A operand of the QK^T MMAs (A-from-TMEM form), q^R (128 x 64) in
+//       shared memory; two 128-column S buffers complete the 512 columns.
+//       Every operand arrives through one ring of 32 KB stages, each one TMA
+//       box of two 128-row x 64-column blocks (one 128-byte-swizzle atom per
+//       block): a tile is 5 stages (4 of c, 1 of k^R), and at a segment start
+//       the 128 query rows of q_cat pass through the same ring (5 stages) on
+//       their way into tensor memory.  The box size matters on B300: an SM's
+//       TMA unit sustains a few boxes per microsecond, so 16 KB boxes cap an
+//       SM near 50 GB/s while 32 KB boxes let half the SMs saturate HBM.
+//       Eight softmax
+//       warps (two threads per query row, 64 tokens each) run the online
+//       softmax, write P (bf16, in the swizzled K-major layout the MMA reads)
+//       and the per-row rescale factor into a local staging buffer, and one
+//       thread moves it into rank 1 with a single bulk shared-to-shared copy
+//       that completes a transaction-counted barrier there.
 //   rank 1 ("value CTA"): O lives in all 512 columns of its tensor memory; it
-//       streams the 512-wide c rows of the same tiles (they are L2 hits right
-//       after rank 0's reads) and issues O += P . C with C read as an
+//       streams the 512-wide c rows of the same tiles in 32-token stages (one
+//       32 KB box each; L2 hits right after rank 0's reads, so HBM sees every
+//       cache byte once) and issues O += P . C with N = 256 and C read as an
 //       MN-major operand straight from the TMA tile.
-// Neither CTA duplicates the other's tensor work, and HBM sees each cache
-// byte once.
+// Neither CTA duplicates the other's tensor work.
 //
 // Online softmax (log2 domain, s2 = s * scale * log2 e).  Each row keeps an
 // INTEGER reference exponent m and l = sum 2^(s2 - m) of the bf16-rounded
@@ -39,49 +48,68 @@
 // segment (a sequence's share of a group's run) leaves O unnormalised plus
 // (m, l) per row; splitkv.cuh merges them.
 //
-// Every wait is bounded (sm100.cuh).  A wait that runs out aborts the CTA's
-// remaining work; the cluster peer notices through its own waits.  Both CTAs
-// meet in a final cluster barrier so neither exits while the other may still
-// touch its shared memory.
+// Every wait is bounded (sm100.cuh), including the exchanges between the two
+// threads of a row, which go through mbarriers rather than bar.sync.  A wait
+// that runs out aborts the CTA's remaining work; the cluster peer notices
+// through its own waits.  Both CTAs meet in a final cluster barrier so neither
+// exits while the other may still touch its shared memory.
 #pragma once
 
 #include "sm100.cuh"
+#include "splitkv.cuh"
 
 namespace mla {
 
-constexpr int kDecThreads = 224;  // 7 warps
-constexpr int kTok = 64;          // cache rows per tile
-constexpr int kStages = 3;
-constexpr int kBlk = kTok * 128;  // one 64-column block of a tile, bytes
-constexpr int kStage0 = 9 * kBlk; // score CTA: 8 c blocks + 1 k^R block
-constexpr int kStage1 = 8 * kBlk; // value CTA: 8 c blocks
-constexpr int kOffP = kStages * kStage1;            // value CTA: P[2] (128 x 64 bf16 each)
+constexpr int kDecThreads = 384;  // 12 warps: 0 TMA, 1 MMA, 2 P copy / release, 4..11 rows
+constexpr int kTok = kTileRows;   // cache rows per tile (128)
+// score CTA (rank 0)
+constexpr int kBlk0 = kTok * 128;          // one block: 128 rows x 64 bf16 = 16 KB
+constexpr int kStage0 = 2 * kBlk0;         // one stage: two blocks (one TMA box)
+constexpr int kStages0 = 5;
+constexpr int kStagesPerTile = 5;          // c: 4 stages, k^R: 1 (q_cat: 4 + 1 for q^R)
+constexpr int kOffQR = kStages0 * kStage0; // q^R: 128 rows x 64 bf16, 128-byte swizzle
+constexpr int kOffPS = kOffQR + 16384;     // P staging: 128 x 128 bf16 + alpha[128]
 constexpr int kPBytes = 128 * kTok * 2;
-constexpr int kOffAlpha = kOffP + 2 * kPBytes;      // value CTA: alpha[2][128] f32
-constexpr int kOffBar = kOffAlpha + 2 * 128 * 4;
-constexpr int kNumBars = 21;
-constexpr uint32_t kPTx = kPBytes + 128 * 4;  // bytes of one P slot + its alpha column
+constexpr uint32_t kPTx = kPBytes + 128 * 4;  // bytes of one P slot with its alpha column
+constexpr int kOffXch = kOffPS + (int)kPTx;   // row max [2 tiles][2 halves][128], row sum [2][128]
+// value CTA (rank 1)
+constexpr int kSub = 32;                   // cache rows per value-CTA stage
+constexpr int kBlk1 = kSub * 128;          // 4 KB
+constexpr int kStage1 = 8 * kBlk1;         // 32 KB
+constexpr int kStages1 = 4;
+constexpr int kOffP = kStages1 * kStage1;  // P slots [2], each P then alpha
+constexpr int kPSlot = 33 * 1024;          // slot stride (keeps P 1 KB aligned)
+// shared by both
+constexpr int kEnd0 = kOffXch + 3072, kEnd1 = kOffP + 2 * kPSlot;
+constexpr int kOffBar = kEnd0 > kEnd1 ? kEnd0 : kEnd1;
+constexpr int kNumBars = 46;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kDecSmem = kOffMisc + 16;
-static_assert(kStages * kStage0 <= kOffBar, "score CTA stages overlap the barriers");
 static_assert(kDecSmem <= 232448, "decode shared memory exceeds 227 KB");
-constexpr uint32_t kQCol = 128;  // score CTA: Q at tensor-memory columns 128..415
+static_assert(kOffQR % 1024 == 0 && kOffPS % 1024 == 0 && kOffP % 1024 == 0 && kPSlot % 1024 == 0,
+              "swizzled operands need 1 KB alignment");
+static_assert(kPTx == (uint32_t)kPBytes + 512 && kPTx % 16 == 0 && kPTx <= (uint32_t)kPSlot,
+              "P slot layout");
+constexpr uint32_t kQCol = 256;  // score CTA: q~ at tensor-memory columns 256..511
 
 // barrier indices
 enum : int {
-  B_FULL = 0, B_EMPTY = 3,           // TMA ring (both CTAs)
-  B_SFULL = 6, B_SEMPTY = 8,         // score CTA: S buffers
-  B_PEMPTY = 10,                     // score CTA: P slot in the value CTA free again
-  B_QREADY = 12,                     // score CTA: Q of the segment is in tensor memory
-  B_PFULL = 13,                      // value CTA: P + alpha of a tile have arrived
-  B_PREADY = 15,                     // value CTA: O rescaled, P may be consumed
-  B_PVDONE = 17,                     // value CTA: P . C of a tile completed
-  B_OFREE = 19,                      // value CTA: epilogue has read O
-  B_DRAIN = 20                       // both: final MMA drain
+  B_FULL = 0, B_EMPTY = 10,          // TMA ring (rank 0: 5 stages, rank 1: 4)
+  B_SFULL = 20, B_SEMPTY = 22,       // score CTA: S buffers
+  B_PEMPTY = 24,                     // score CTA: P slot in the value CTA free again
+  B_QREADY = 26,                     // score CTA: Q of the segment is in place
+  B_XCH = 27,                        // score CTA: row-max exchange [tile parity][quadrant]
+  B_XL = 35,                         // score CTA: row-sum exchange at a segment end
+  B_PSTAGED = 36,                    // score CTA: P of a tile is in the staging buffer
+  B_PSFREE = 37,                     // score CTA: staging buffer read by the copy
+  B_PFULL = 38,                      // value CTA: P + alpha of a tile have arrived
+  B_PREADY = 40,                     // value CTA: O rescaled, P may be consumed
+  B_PVDONE = 42,                     // value CTA: P . C of a tile completed
+  B_OFREE = 44,                      // value CTA: epilogue has read O
+  B_DRAIN = 45                       // both: final MMA drain
 };
 
 struct DecodeParams {
-  const __nv_bfloat16* q_cat;  // [B,S,H,576]
   const int32_t* seqlens;      // [B]
   const int32_t* prefix;       // plan (splitkv.cuh)
   const int32_t* gfirst;
@@ -98,6 +126,7 @@ struct DecodeParams {
 
 struct TileInfo {
   int b, t, L, i, k, slot;
+  int nvt;  // cache rows of the sequence inside this tile (1..128)
   bool first, last;
 };
 
@@ -117,11 +146,18 @@ __device__ __forceinline__ void for_each_tile(const DecodeParams& p, int g, F&& 
     const int slot = p.segbase[b] + (g - p.gfirst[b]);
     const int L = p.seqlens[b];
     for (int t = tb; t < te; ++t, ++i) {
-      const TileInfo ti{b, t, L, i, k, slot, t == tb, t == te - 1};
+      const TileInfo ti{b, t, L, i, k, slot, min(L - t * kTok, kTok), t == tb, t == te - 1};
       if (!f(ti)) return;
     }
     ++k;
   }
+}
+
+// Score-CTA ring position of stage j of tile i in segment k: every segment
+// first sends its 5 query stages through the ring, every tile its 5 cache stages.
+__device__ __forceinline__ int ring_q_stage(int i, int k, int j) { return kStagesPerTile * (i + k) + j; }
+__device__ __forceinline__ int ring_kv_stage(int i, int k, int j) {
+  return kStagesPerTile * (i + k + 1) + j;
 }
 
 // All 32 lanes wait; the outcome is made warp-uniform so that warp-collective
@@ -136,13 +172,15 @@ __device__ __forceinline__ float exp2_int(int d) {
 }
 
 __global__ void __launch_bounds__(kDecThreads, 1)
-    decode_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_kr,
-                  const DecodeParams p) {
+    decode_kernel(const __grid_constant__ CUtensorMap tm_c0, const __grid_constant__ CUtensorMap tm_kr,
+                  const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_qr,
+                  const __grid_constant__ CUtensorMap tm_c1, const DecodeParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t rank = cluster_ctarank();
   const int cluster = blockIdx.x >> 1;
   const int rb = cluster % p.n_rb, g = cluster / p.n_rb;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int SH = p.S * p.H;
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kOffBar);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile uint32_t* abort_flag = tmem_slot + 1;
@@ -154,28 +192,38 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       *abort_flag = 1u;
       atomicOr(p.status, kDevErrInternal);
     }
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kStages0; ++s) {
       mbar_init(&bar[B_FULL + s], 1);
       mbar_init(&bar[B_EMPTY + s], 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bar[B_SFULL + s], 1);
-      mbar_init(&bar[B_SEMPTY + s], 128);
+      mbar_init(&bar[B_SEMPTY + s], 256);
       mbar_init(&bar[B_PEMPTY + s], 1);
       mbar_init(&bar[B_PFULL + s], 1);
-      mbar_init(&bar[B_PREADY + s], 128);
+      mbar_init(&bar[B_PREADY + s], 256);
       mbar_init(&bar[B_PVDONE + s], 1);
     }
-    mbar_init(&bar[B_QREADY], 128);
-    mbar_init(&bar[B_OFREE], 128);
+    for (int s = 0; s < 8; ++s) mbar_init(&bar[B_XCH + s], 64);
+    mbar_init(&bar[B_QREADY], 256);
+    mbar_init(&bar[B_XL], 256);
+    mbar_init(&bar[B_PSTAGED], 256);
+    mbar_init(&bar[B_PSFREE], 1);
+    mbar_init(&bar[B_OFREE], 256);
     mbar_init(&bar[B_DRAIN], 1);
     if (rank == 1) {  // first phase of each P slot expects one slot's bytes
       mbar_arrive_expect_tx(&bar[B_PFULL + 0], kPTx);
       mbar_arrive_expect_tx(&bar[B_PFULL + 1], kPTx);
     }
     fence_mbar_init_cluster();
-    tma_prefetch_desc(&tm_c);
-    tma_prefetch_desc(&tm_kr);
+    if (rank == 0) {
+      tma_prefetch_desc(&tm_c0);
+      tma_prefetch_desc(&tm_kr);
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_qr);
+    } else {
+      tma_prefetch_desc(&tm_c1);
+    }
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, 512);
@@ -191,72 +239,116 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   if (run && warp == 0) {
     // ------------------------------------------------ TMA producer (both CTAs)
     if (lane == 0) {
-      const uint32_t sbytes = rank == 0 ? kStage0 : kStage1;
-      int last_use[kStages] = {-1, -1, -1};
+      int last_use[kStages0];
+      for (int s = 0; s < kStages0; ++s) last_use[s] = -1;
+      const int nst = rank == 0 ? kStages0 : kStages1;
+      int q = 0;  // running stage counter
       for_each_tile(p, g, [&](const TileInfo& ti) {
-        const int st = ti.i % kStages;
-        const uint32_t ph = (uint32_t)(ti.i / kStages) & 1u;
-        if (!mbar_wait(&bar[B_EMPTY + st], ph ^ 1u, wc)) return false;
-        uint8_t* dst = smem + st * sbytes;
-        mbar_arrive_expect_tx(&bar[B_FULL + st], sbytes);
         const int row0 = ti.b * p.Lmax + ti.t * kTok;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) tma_load_2d(dst + j * kBlk, &tm_c, &bar[B_FULL + st], j * 64, row0);
-        if (rank == 0) tma_load_2d(dst + 8 * kBlk, &tm_kr, &bar[B_FULL + st], 0, row0);
-        last_use[st] = ti.i;
+        if (rank == 0) {
+          const int nstg = ti.first ? 2 * kStagesPerTile : kStagesPerTile;
+          const int qrow0 = ti.b * SH + rb * 128;
+          for (int j = 0; j < nstg; ++j, ++q) {
+            const int st = q % nst;
+            if (!mbar_wait(&bar[B_EMPTY + st], ((uint32_t)(q / nst) & 1u) ^ 1u, wc)) return false;
+            uint8_t* dst = smem + st * kStage0;
+            const int jj = ti.first ? j - kStagesPerTile : j;  // < 0: a query stage
+            const bool single = (jj == 4) || (jj == -1);      // k^R or q^R: one block
+            mbar_arrive_expect_tx(&bar[B_FULL + st], single ? kBlk0 : kStage0);
+            if (jj < -1)
+              tma_load_3d(dst, &tm_q, &bar[B_FULL + st], 0, qrow0, 2 * j);
+            else if (jj == -1)
+              tma_load_2d(dst, &tm_qr, &bar[B_FULL + st], 512, qrow0);
+            else if (jj < 4)
+              tma_load_3d(dst, &tm_c0, &bar[B_FULL + st], 0, row0, 2 * jj);
+            else
+              tma_load_2d(dst, &tm_kr, &bar[B_FULL + st], 0, row0);
+            last_use[st] = q;
+          }
+        } else {
+          const int nsub = (ti.nvt + kSub - 1) / kSub;
+          for (int u = 0; u < nsub; ++u, ++q) {  // 32-row stages of the 512 c columns
+            const int st = q % nst;
+            if (!mbar_wait(&bar[B_EMPTY + st], ((uint32_t)(q / nst) & 1u) ^ 1u, wc)) return false;
+            uint8_t* dst = smem + st * kStage1;
+            mbar_arrive_expect_tx(&bar[B_FULL + st], kStage1);
+            tma_load_3d(dst, &tm_c1, &bar[B_FULL + st], 0, row0 + u * kSub, 0);
+            last_use[st] = q;
+          }
+        }
         return true;
       });
-      for (int s = 0; s < kStages; ++s)  // let every issued copy land before the CTA winds down
-        if (last_use[s] >= 0) mbar_wait_drain(&bar[B_FULL + s], (uint32_t)(last_use[s] / kStages) & 1u, wc);
+      for (int s = 0; s < nst; ++s)  // let every issued copy land before the CTA winds down
+        if (last_use[s] >= 0) mbar_wait_drain(&bar[B_FULL + s], (uint32_t)(last_use[s] / nst) & 1u, wc);
     }
   } else if (run && warp == 1) {
     // ------------------------------------------------ MMA issuer (one thread)
     if (lane == 0) {
       if (rank == 0) {
         constexpr uint32_t idesc = idesc_bf16_f32(128, kTok, 0, 0);
+        const uint32_t qr = smem_u32(smem + kOffQR);
         for_each_tile(p, g, [&](const TileInfo& ti) {
-          const int st = ti.i % kStages, slot = ti.i & 1;
-          const uint32_t ph = (uint32_t)(ti.i / kStages) & 1u, sph = (uint32_t)(ti.i >> 1) & 1u;
-          if (!mbar_wait(&bar[B_FULL + st], ph, wc)) return false;
+          const int slot = ti.i & 1;
+          const uint32_t sph = (uint32_t)(ti.i >> 1) & 1u;
+          if (ti.first) {  // the query stages have been moved out of the ring: release them
+            if (!mbar_wait(&bar[B_QREADY], (uint32_t)ti.k & 1u, wc)) return false;
+            for (int j = 0; j < kStagesPerTile; ++j)
+              mbar_arrive(&bar[B_EMPTY + ring_q_stage(ti.i, ti.k, j) % kStages0]);
+          }
           if (!mbar_wait(&bar[B_SEMPTY + slot], sph ^ 1u, wc)) return false;
-          if (ti.first && !mbar_wait(&bar[B_QREADY], (uint32_t)ti.k & 1u, wc)) return false;
-          tc_fence_after();
-          const uint32_t sbase = smem_u32(smem + st * kStage0);
           const uint32_t d = tmem + (uint32_t)slot * kTok;
-#pragma unroll 4
-          for (int kk = 0; kk < 36; ++kk) {  // K = 576 in steps of 16
-            const uint64_t bd = smem_desc(sbase + (kk >> 2) * kBlk + (kk & 3) * 32, 16, 1024, 2);
-            mma_ts(d, tmem + kQCol + (uint32_t)kk * 8, bd, idesc, kk > 0 ? 1u : 0u);
+          for (int j = 0; j < kStagesPerTile; ++j) {
+            const int q = ring_kv_stage(ti.i, ti.k, j), st = q % kStages0;
+            if (!mbar_wait(&bar[B_FULL + st], (uint32_t)(q / kStages0) & 1u, wc)) return false;
+            tc_fence_after();
+            const uint32_t sbase = smem_u32(smem + st * kStage0);
+            if (j < 4) {
+#pragma unroll
+              for (int kk = 0; kk < 8; ++kk) {  // 2 blocks x 4 K-steps of 16
+                const int gk = j * 8 + kk;
+                const uint64_t bd = smem_desc(sbase + (kk >> 2) * kBlk0 + (kk & 3) * 32, 16, 1024, 2);
+                mma_ts(d, tmem + kQCol + (uint32_t)gk * 8, bd, idesc, gk > 0 ? 1u : 0u);
+              }
+            } else {
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)  // k^R against q^R from shared memory
+                mma_ss(d, smem_desc(qr + kk * 32, 16, 1024, 2), smem_desc(sbase + kk * 32, 16, 1024, 2),
+                       idesc, 1u);
+            }
+            mma_commit(&bar[B_EMPTY + st]);
           }
           mma_commit(&bar[B_SFULL + slot]);
-          mma_commit(&bar[B_EMPTY + st]);
           return true;
         });
       } else {
         constexpr uint32_t idesc = idesc_bf16_f32(128, 256, 0, 1);
+        int q = 0;
         for_each_tile(p, g, [&](const TileInfo& ti) {
-          const int st = ti.i % kStages, slot = ti.i & 1;
-          const uint32_t ph = (uint32_t)(ti.i / kStages) & 1u, sph = (uint32_t)(ti.i >> 1) & 1u;
-          if (!mbar_wait(&bar[B_FULL + st], ph, wc)) return false;
+          const int slot = ti.i & 1;
+          const uint32_t sph = (uint32_t)(ti.i >> 1) & 1u;
           if (!mbar_wait(&bar[B_PREADY + slot], sph, wc)) return false;
           if (ti.first && ti.k > 0 && !mbar_wait(&bar[B_OFREE], (uint32_t)(ti.k - 1) & 1u, wc))
             return false;
-          fence_proxy_async_cta();  // P arrived through the generic proxy; the MMA reads it
-          tc_fence_after();
-          const int nvt = min(ti.L - ti.t * kTok, kTok);
-          const int nk = (nvt + 15) >> 4;
-          const uint32_t sbase = smem_u32(smem + st * kStage1);
-          const uint32_t pbase = smem_u32(smem + kOffP + slot * kPBytes);
-          for (int kt = 0; kt < nk; ++kt) {  // K = tokens in steps of 16
-            const uint64_t ad = smem_desc(pbase + kt * 32, 16, 1024, 2);
+          fence_proxy_async_cta();  // tail rows were zeroed through the generic proxy
+          const int nk = (ti.nvt + 15) >> 4;  // K-steps of 16 tokens
+          const uint32_t pbase = smem_u32(smem + kOffP + slot * kPSlot);
+          for (int u = 0; u * 2 < nk; ++u, ++q) {
+            const int st = q % kStages1;
+            if (!mbar_wait(&bar[B_FULL + st], (uint32_t)(q / kStages1) & 1u, wc)) return false;
+            tc_fence_after();
+            const uint32_t sbase = smem_u32(smem + st * kStage1);
+            for (int kt = 0; kt < 2 && u * 2 + kt < nk; ++kt) {
+              const int gk = u * 2 + kt;
+              const uint64_t ad = smem_desc(pbase + (gk >> 2) * 16384 + (gk & 3) * 32, 16, 1024, 2);
 #pragma unroll
-            for (int n = 0; n < 2; ++n) {   // N = 512 latent columns as 2 x 256
-              const uint64_t bd = smem_desc(sbase + n * 4 * kBlk + kt * 2048, kBlk, 1024, 2);
-              mma_ss(tmem + (uint32_t)n * 256, ad, bd, idesc, (kt > 0 || !ti.first) ? 1u : 0u);
+              for (int n = 0; n < 2; ++n) {  // N = 512 latent columns as 2 x 256
+                const uint64_t bd = smem_desc(sbase + n * 4 * kBlk1 + kt * 2048, kBlk1, 1024, 2);
+                mma_ss(tmem + (uint32_t)n * 256, ad, bd, idesc, (gk > 0 || !ti.first) ? 1u : 0u);
+              }
             }
+            mma_commit(&bar[B_EMPTY + st]);
           }
           mma_commit(&bar[B_PVDONE + slot]);
-          mma_commit(&bar[B_EMPTY + st]);
           return true;
         });
       }
@@ -264,49 +356,73 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       mbar_wait_drain(&bar[B_DRAIN], 0, wc);
     }
   } else if (run && warp == 2) {
-    // ------------------------------------------------ value CTA: P-slot releaser
-    if (rank == 1 && lane == 0) {
-      for_each_tile(p, g, [&](const TileInfo& ti) {
-        const int slot = ti.i & 1;
-        if (!mbar_wait(&bar[B_PVDONE + slot], (uint32_t)(ti.i >> 1) & 1u, wc)) return false;
-        mbar_arrive_remote(&bar[B_PEMPTY + slot], 0);
-        return true;
-      });
+    if (lane == 0) {
+      if (rank == 0) {
+        // -------------------------------------------- score CTA: P copy into the value CTA
+        const uint32_t p_remote = map_to_cta(smem_u32(smem + kOffP), 1);
+        const uint32_t pfull_remote = map_to_cta(smem_u32(&bar[B_PFULL]), 1);
+        for_each_tile(p, g, [&](const TileInfo& ti) {
+          const int slot = ti.i & 1;
+          const uint32_t sph = (uint32_t)(ti.i >> 1) & 1u;
+          if (!mbar_wait(&bar[B_PSTAGED], (uint32_t)ti.i & 1u, wc)) return false;
+          if (!mbar_wait(&bar[B_PEMPTY + slot], sph ^ 1u, wc)) return false;
+          bulk_copy_to_peer(p_remote + (uint32_t)(slot * kPSlot), smem + kOffPS, kPTx,
+                            pfull_remote + (uint32_t)slot * 8);
+          bulk_commit_group();
+          bulk_wait_group_read0();
+          mbar_arrive(&bar[B_PSFREE]);
+          return true;
+        });
+      } else {
+        // -------------------------------------------- value CTA: P-slot releaser
+        for_each_tile(p, g, [&](const TileInfo& ti) {
+          const int slot = ti.i & 1;
+          if (!mbar_wait(&bar[B_PVDONE + slot], (uint32_t)(ti.i >> 1) & 1u, wc)) return false;
+          mbar_arrive_remote(&bar[B_PEMPTY + slot], 0);
+          return true;
+        });
+      }
     }
-  } else if (run) {
-    // ------------------------------------------------ warps 3..6: one row per thread
-    const int q = warp & 3;
-    const int r = q * 32 + lane;
-    const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16);
-    const int SH = p.S * p.H;
+  } else if (run && warp >= 4) {
+    // ------------------------------------------------ warps 4..11: two threads per row
+    const int q4 = warp & 3;          // tensor-memory lane quadrant of this warp
+    const int hf = (warp - 4) >> 2;   // half of the row's columns this thread owns
+    const int r = q4 * 32 + lane;
+    const uint32_t tl = tmem + ((uint32_t)(q4 * 32) << 16);
     const int gr = rb * 128 + r;
     const bool valid = gr < SH;
-    const int s_r = valid ? gr / p.H : 0, h_r = valid ? gr - (gr / p.H) * p.H : 0;
+    const int s_r = valid ? gr / p.H : 0;
 
     if (rank == 0) {
       // ---------------------------------------- scores + online softmax
-      const uint32_t p_remote = map_to_cta(smem_u32(smem + kOffP), 1);
-      const uint32_t a_remote = map_to_cta(smem_u32(smem + kOffAlpha), 1);
-      const uint32_t pfull_remote = map_to_cta(smem_u32(&bar[B_PFULL]), 1);
+      float* xch = reinterpret_cast<float*>(smem + kOffXch);  // [2][2][128], then l [2][128]
+      uint8_t* ps = smem + kOffPS;
       float m_ref = -INFINITY, l = 0.f;
       int limit = 0;
       for_each_tile(p, g, [&](const TileInfo& ti) {
-        if (ti.first) {  // the previous segment's MMAs are done: load this segment's Q
+        if (ti.first) {
+          // q~ into tensor memory (this thread: 4 of its row's 8 blocks), q^R
+          // into its own buffer; the blocks come through the ring.
           limit = valid ? ti.L - p.S + s_r + 1 : 0;
-          const uint4* qrow = reinterpret_cast<const uint4*>(
-              p.q_cat + (((size_t)ti.b * p.S + s_r) * p.H + h_r) * 576);
-#pragma unroll 1
-          for (int c3 = 0; c3 < 9; c3 += 3) {  // 3 x 3 chunks: 24 loads in flight per thread
-            uint32_t v[3][32];
+          for (int j = hf * 4; j < hf * 4 + 4 + hf; ++j) {  // block j of the query row
+            const int q = ring_q_stage(ti.i, ti.k, j >> 1), st = q % kStages0;
+            if (!warp_wait(&bar[B_FULL + st], (uint32_t)(q / kStages0) & 1u, wc)) return false;
+            const uint8_t* rowp = smem + st * kStage0 + (j & 1) * kBlk0 + r * 128;
+            if (j < 8) {
+              uint32_t v[32];
 #pragma unroll
-            for (int c = 0; c < 3; ++c)
-#pragma unroll
-              for (int u = 0; u < 8; ++u) {
-                const uint4 x = valid ? __ldg(qrow + (c3 + c) * 8 + u) : make_uint4(0, 0, 0, 0);
-                v[c][4 * u] = x.x; v[c][4 * u + 1] = x.y; v[c][4 * u + 2] = x.z; v[c][4 * u + 3] = x.w;
+              for (int ch = 0; ch < 8; ++ch) {  // logical chunk ch sits at ch ^ (r & 7)
+                const uint4 x = *reinterpret_cast<const uint4*>(rowp + ((ch ^ (r & 7)) << 4));
+                v[4 * ch] = x.x; v[4 * ch + 1] = x.y; v[4 * ch + 2] = x.z; v[4 * ch + 3] = x.w;
               }
+              tmem_st32(tl + kQCol + (uint32_t)j * 32, v);
+            } else {  // q^R keeps the same swizzled row layout
 #pragma unroll
-            for (int c = 0; c < 3; ++c) tmem_st32(tl + kQCol + (uint32_t)(c3 + c) * 32, v[c]);
+              for (int ch = 0; ch < 8; ++ch)
+                *reinterpret_cast<uint4*>(smem + kOffQR + r * 128 + ch * 16) =
+                    *reinterpret_cast<const uint4*>(rowp + ch * 16);
+              fence_proxy_async_cta();
+            }
           }
           tmem_wait_st();
           tc_fence_before();
@@ -322,21 +438,24 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         {
           uint32_t (&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[0]);
           uint32_t (&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[32]);
-          tmem_ld32(tl + (uint32_t)slot * kTok, lo);
-          tmem_ld32(tl + (uint32_t)slot * kTok + 32, hi);
+          tmem_ld32(tl + (uint32_t)(slot * kTok + hf * 64), lo);
+          tmem_ld32(tl + (uint32_t)(slot * kTok + hf * 64 + 32), hi);
         }
         tmem_wait_ld();
         tc_fence_before();
         mbar_arrive(&bar[B_SEMPTY + slot]);
 
-        const int nv = min(max(limit - ti.t * kTok, 0), kTok);
-        float mx = -INFINITY;
+        const int nv = min(max(limit - ti.t * kTok - hf * 64, 0), 64);
+        float mx = -INFINITY;  // max of the raw scores; the scale is positive
 #pragma unroll
-        for (int c = 0; c < kTok; ++c) {
-          const float s2 = __uint_as_float(sv[c]) * p.scale_log2;
-          sv[c] = __float_as_uint(s2);
-          if (c < nv) mx = fmaxf(mx, s2);
-        }
+        for (int c = 0; c < 64; ++c)
+          if (c < nv) mx = fmaxf(mx, __uint_as_float(sv[c]));
+        mx *= p.scale_log2;
+        // both threads of the row (same quadrant, warps q4 and q4 + 4) take the same maximum
+        xch[(slot * 2 + hf) * 128 + r] = mx;
+        mbar_arrive(&bar[B_XCH + slot * 4 + q4]);
+        if (!warp_wait(&bar[B_XCH + slot * 4 + q4], sph, wc)) return false;
+        mx = fmaxf(mx, xch[(slot * 2 + (hf ^ 1)) * 128 + r]);
         float alpha = 1.f;
         if (mx > m_ref + 8.f) {
           const float mn = ceilf(mx);
@@ -346,37 +465,54 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         }
         const float mu = (m_ref == -INFINITY) ? 0.f : m_ref;
         uint32_t pk[32];
-        float lsum = 0.f;
+        float lsum0 = 0.f, lsum1 = 0.f;
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const float e0 = (2 * c < nv) ? exp2f(__uint_as_float(sv[2 * c]) - mu) : 0.f;
-          const float e1 = (2 * c + 1 < nv) ? exp2f(__uint_as_float(sv[2 * c + 1]) - mu) : 0.f;
+        for (int c = 0; c < 32; ++c) {  // 2^(s * scale * log2 e - m)
+          const float e0 = (2 * c < nv) ? ex2_approx(fmaf(__uint_as_float(sv[2 * c]), p.scale_log2, -mu)) : 0.f;
+          const float e1 =
+              (2 * c + 1 < nv) ? ex2_approx(fmaf(__uint_as_float(sv[2 * c + 1]), p.scale_log2, -mu)) : 0.f;
           pk[c] = pack_bf16x2(e0, e1);
           const __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162*>(&pk[c]);
-          lsum += __low2float(b2) + __high2float(b2);
+          lsum0 += __low2float(b2);
+          lsum1 += __high2float(b2);
         }
-        l += lsum;
+        l += lsum0 + lsum1;
 
-        if (!warp_wait(&bar[B_PEMPTY + slot], sph ^ 1u, wc)) return false;
-        const uint32_t row = p_remote + (uint32_t)slot * kPBytes + (uint32_t)r * 128;
-        const uint32_t rbar = pfull_remote + (uint32_t)slot * 8;
+        // the staging buffer is free once the previous tile's copy has read it
+        if (!warp_wait(&bar[B_PSFREE], ((uint32_t)ti.i & 1u) ^ 1u, wc)) return false;
+        uint8_t* row = ps + hf * 16384 + r * 128;
 #pragma unroll
         for (int ch = 0; ch < 8; ++ch)  // 128-byte swizzle: chunk ch of row r sits at ch ^ (r & 7)
-          st_async_v4(row + (uint32_t)((ch ^ (r & 7)) << 4),
-                      make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]), rbar);
-        st_async_f32(a_remote + (uint32_t)(slot * 128 + r) * 4, alpha, rbar);
-        if (ti.last && valid) p.ml[((size_t)ti.slot * p.n_rb + rb) * 128 + r] = make_float2(mu, l);
+          *reinterpret_cast<uint4*>(row + ((ch ^ (r & 7)) << 4)) =
+              make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+        if (hf == 0) reinterpret_cast<float*>(ps + kPBytes)[r] = alpha;
+        fence_proxy_async_cta();  // the bulk copy reads the buffer through the async proxy
+        mbar_arrive(&bar[B_PSTAGED]);
+        if (ti.last) {  // segment end: add the two halves' sums, write (m, l)
+          float* xl = xch + 512;  // [2][128]
+          xl[hf * 128 + r] = l;
+          mbar_arrive(&bar[B_XL]);
+          if (!warp_wait(&bar[B_XL], (uint32_t)ti.k & 1u, wc)) return false;
+          if (hf == 0 && valid)
+            p.ml[((size_t)ti.slot * p.n_rb + rb) * 128 + r] = make_float2(mu, l + xl[128 + r]);
+          // the next segment's exchange reuses xl only after its own tiles'
+          // row-max exchanges, which both threads pass after reading it here
+        }
         return true;
       });
     } else {
       // ---------------------------------------- rescale, tail zeroing, epilogue
-      const int wt = threadIdx.x - 96;  // 0..127
-      const volatile float* alpha_buf = reinterpret_cast<const volatile float*>(smem + kOffAlpha);
+      const int wt = threadIdx.x - 128;  // 0..255
+      int q = 0;  // running stage counter (as the producer's)
       for_each_tile(p, g, [&](const TileInfo& ti) {
-        const int slot = ti.i & 1, st = ti.i % kStages;
-        const uint32_t sph = (uint32_t)(ti.i >> 1) & 1u, ph = (uint32_t)(ti.i / kStages) & 1u;
+        const int slot = ti.i & 1;
+        const uint32_t sph = (uint32_t)(ti.i >> 1) & 1u;
+        const int nsub = (ti.nvt + kSub - 1) / kSub;
+        const int q0 = q;
+        q += nsub;
         if (!warp_wait(&bar[B_PFULL + slot], sph, wc)) return false;
-        const float alpha = alpha_buf[slot * 128 + r];
+        const float alpha =
+            reinterpret_cast<const volatile float*>(smem + kOffP + slot * kPSlot + kPBytes)[r];
         if (wt == 0) mbar_arrive_expect_tx(&bar[B_PFULL + slot], kPTx);  // arm the slot's next phase
         const bool need = !ti.first && alpha != 1.f;
         if (__any_sync(0xffffffffu, need)) {
@@ -384,28 +520,29 @@ __global__ void __launch_bounds__(kDecThreads, 1)
           if (!warp_wait(&bar[B_PVDONE + (slot ^ 1)], (uint32_t)((ti.i - 1) >> 1) & 1u, wc)) return false;
           tc_fence_after();
 #pragma unroll 1
-          for (int c = 0; c < 16; ++c) {
+          for (int c = 0; c < 8; ++c) {
             uint32_t v[32];
-            tmem_ld32(tl + (uint32_t)c * 32, v);
+            const uint32_t a = tl + (uint32_t)(hf * 256 + c * 32);
+            tmem_ld32(a, v);
             tmem_wait_ld();
             if (need) {
 #pragma unroll
               for (int u = 0; u < 32; ++u) v[u] = __float_as_uint(__uint_as_float(v[u]) * alpha);
             }
-            tmem_st32(tl + (uint32_t)c * 32, v);
+            tmem_st32(a, v);
           }
           tmem_wait_st();
         }
-        const int nvt = min(ti.L - ti.t * kTok, kTok);
-        if (nvt & 15) {
+        if (ti.nvt & 15) {
           // cache rows past the sequence end inside the last 16-row MMA step hold
           // arbitrary bytes; their weights are 0 but 0 * NaN is not, so zero them
-          if (!warp_wait(&bar[B_FULL + st], ph, wc)) return false;
-          const int z0 = nvt, nzr = ((nvt + 15) & ~15) - nvt;
+          const int u = ti.nvt / kSub, qs = q0 + u, st = qs % kStages1;
+          if (!warp_wait(&bar[B_FULL + st], (uint32_t)(qs / kStages1) & 1u, wc)) return false;
+          const int z0 = ti.nvt - u * kSub, nzr = ((ti.nvt + 15) & ~15) - ti.nvt;
           uint8_t* sb = smem + st * kStage1;
-          for (int idx = wt; idx < nzr * 64; idx += 128) {
+          for (int idx = wt; idx < nzr * 64; idx += 256) {
             const int blk = idx / (nzr * 8), rem = idx - blk * (nzr * 8);
-            *reinterpret_cast<uint4*>(sb + blk * kBlk + (z0 + (rem >> 3)) * 128 + (rem & 7) * 16) =
+            *reinterpret_cast<uint4*>(sb + blk * kBlk1 + (z0 + (rem >> 3)) * 128 + (rem & 7) * 16) =
                 make_uint4(0, 0, 0, 0);
           }
           fence_proxy_async_cta();
@@ -415,17 +552,22 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         if (ti.last) {
           if (!warp_wait(&bar[B_PVDONE + slot], sph, wc)) return false;
           tc_fence_after();
-          // column-major [512][128]: for each column a warp stores 32 consecutive floats
+          // O partial, column-major [512][128] f32: for each column a warp
+          // stores 32 consecutive floats.  Two 32-column loads per wait keep
+          // more stores in flight.
           float* dst = p.opart + ((size_t)ti.slot * p.n_rb + rb) * 512 * 128 + r;
 #pragma unroll 1
-          for (int c = 0; c < 16; ++c) {
-            uint32_t v[32];
-            tmem_ld32(tl + (uint32_t)c * 32, v);
-            tmem_wait_ld();
-            if (valid) {
-#pragma unroll
-              for (int u = 0; u < 32; ++u) dst[(size_t)(c * 32 + u) * 128] = __uint_as_float(v[u]);
+          for (int c = 0; c < 4; ++c) {
+            uint32_t v[64];
+            {
+              uint32_t (&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[0]);
+              uint32_t (&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[32]);
+              tmem_ld32(tl + (uint32_t)(hf * 256 + c * 64), lo);
+              tmem_ld32(tl + (uint32_t)(hf * 256 + c * 64 + 32), hi);
             }
+            tmem_wait_ld();
+#pragma unroll
+            for (int u = 0; u < 64; ++u) dst[(size_t)(hf * 256 + c * 64 + u) * 128] = __uint_as_float(v[u]);
           }
           tc_fence_before();
           mbar_arrive(&bar[B_OFREE]);

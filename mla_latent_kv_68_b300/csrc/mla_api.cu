@@ -97,6 +97,31 @@ bool encode_tiled(CUtensorMap* map, const void* base, cuuint32_t rank, const cuu
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Tensor maps of the decode kernel: the score CTA reads 128-row boxes of c
+// and k^R, the value CTA 32-row boxes of c (64 columns = 128 bytes each, the
+// width of one 128-byte-swizzle atom).
+struct DecodeMaps {
+  CUtensorMap c0, kr, q, qr, c1;
+};
+
+// c_kv and q_cat rows are also seen as [rows][blocks of 64 columns] so that
+// one 3-D box brings several 128-byte-swizzle atoms at once: an SM's TMA unit
+// sustains a few boxes per microsecond, so large boxes are what reach HBM
+// bandwidth.
+bool encode_decode_maps(DecodeMaps* m, const void* q_cat, const void* c_kv, const void* k_r,
+                        int B, int S, int H, int Lmax) {
+  const cuuint64_t rows = (cuuint64_t)B * Lmax, qrows = (cuuint64_t)B * S * H;
+  const cuuint64_t c3d[3] = {64, rows, 8}, c3s[2] = {1024, 128};
+  const cuuint32_t c0b[3] = {64, (cuuint32_t)mla::kTok, 2}, c1b[3] = {64, (cuuint32_t)mla::kSub, 8};
+  const cuuint64_t kd[2] = {64, rows}, ks[1] = {128};
+  const cuuint32_t b2[2] = {64, (cuuint32_t)mla::kTok};
+  const cuuint64_t q3d[3] = {64, qrows, 9}, q3s[2] = {1152, 128};
+  const cuuint64_t qd[2] = {576, qrows}, qs[1] = {1152};
+  return encode_tiled(&m->c0, c_kv, 3, c3d, c3s, c0b) && encode_tiled(&m->kr, k_r, 2, kd, ks, b2) &&
+         encode_tiled(&m->q, q_cat, 3, q3d, q3s, c0b) && encode_tiled(&m->qr, q_cat, 2, qd, qs, b2) &&
+         encode_tiled(&m->c1, c_kv, 3, c3d, c3s, c1b);
+}
+
 // Workspace layout of mla_decode / mla_splitkv_combine.
 struct WsLayout {
   int n_rb = 0, G = 0, slots = 0;
@@ -231,7 +256,7 @@ mla_status mla_decode(const mla_bf16* q_cat, const mla_bf16* c_kv, const mla_bf1
   if (B < 1 || S < 1 || H < 1 || Lmax < 1 || !(softmax_scale > 0.f) || !std::isfinite(softmax_scale))
     return MLA_ERR_INVALID_ARG;
   if (!decode_shape_ok(B, S, H)) return MLA_ERR_UNSUPPORTED;
-  if ((long long)B * Lmax + 64 > 0x7fffffffLL) return MLA_ERR_UNSUPPORTED;
+  if ((long long)B * Lmax + mla::kTok > 0x7fffffffLL) return MLA_ERR_UNSUPPORTED;
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return MLA_ERR_WORKSPACE;
   const DeviceInfo* dev = device_info();
   if (!dev) return MLA_ERR_CUDA;
@@ -255,17 +280,10 @@ mla_status mla_decode(const mla_bf16* q_cat, const mla_bf16* c_kv, const mla_bf1
   mla::plan_kernel<<<1, 1024, 0, st>>>(pp);
   if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
 
-  CUtensorMap tc, tk;
-  const cuuint64_t cd[2] = {512, (cuuint64_t)B * Lmax};
-  const cuuint64_t cs[1] = {1024};
-  const cuuint32_t cb[2] = {64, 64};
-  const cuuint64_t kd[2] = {64, (cuuint64_t)B * Lmax};
-  const cuuint64_t ks[1] = {128};
-  if (!encode_tiled(&tc, c_kv, 2, cd, cs, cb) || !encode_tiled(&tk, k_r, 2, kd, ks, cb))
-    return MLA_ERR_INVALID_ARG;
+  DecodeMaps maps;
+  if (!encode_decode_maps(&maps, q_cat, c_kv, k_r, B, S, H, Lmax)) return MLA_ERR_INVALID_ARG;
 
   mla::DecodeParams p;
-  p.q_cat = reinterpret_cast<const __nv_bfloat16*>(q_cat);
   p.seqlens = seqlens;
   p.prefix = pp.prefix;
   p.gfirst = pp.gfirst;
@@ -296,7 +314,9 @@ mla_status mla_decode(const mla_bf16* q_cat, const mla_bf16* c_kv, const mla_bf1
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, mla::decode_kernel, tc, tk, p) != cudaSuccess) return MLA_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, mla::decode_kernel, maps.c0, maps.kr, maps.q, maps.qr, maps.c1, p) !=
+      cudaSuccess)
+    return MLA_ERR_CUDA;
   return launch_status();
 }
 
@@ -312,6 +332,8 @@ mla_status mla_splitkv_combine(const void* workspace, size_t workspace_bytes, ml
   if (workspace_bytes < w.total) return MLA_ERR_WORKSPACE;
   const uint8_t* ws = static_cast<const uint8_t*>(workspace);
   mla::CombineParams p;
+  p.prefix = reinterpret_cast<const int32_t*>(ws + w.prefix);
+  p.gfirst = reinterpret_cast<const int32_t*>(ws + w.gfirst);
   p.segbase = reinterpret_cast<const int32_t*>(ws + w.segbase);
   p.ml = reinterpret_cast<const float2*>(ws + w.ml);
   p.opart = reinterpret_cast<const float*>(ws + w.opart);
@@ -321,6 +343,7 @@ mla_status mla_splitkv_combine(const void* workspace, size_t workspace_bytes, ml
   p.S = S;
   p.H = H;
   p.n_rb = w.n_rb;
+  p.G = w.G;
   const dim3 grid((unsigned)(B * w.n_rb), 8);
   mla::combine_kernel<<<grid, 128, 0, (cudaStream_t)stream>>>(p);
   return launch_status();
@@ -422,7 +445,7 @@ extern "C" mla_status mla_decode_noalloc(const mla_bf16* q_cat, const mla_bf16* 
   if (B < 1 || S < 1 || H < 1 || Lmax < 1 || !(softmax_scale > 0.f) || !std::isfinite(softmax_scale))
     return MLA_ERR_INVALID_ARG;
   if (!decode_shape_ok(B, S, H)) return MLA_ERR_UNSUPPORTED;
-  if ((long long)B * Lmax + 64 > 0x7fffffffLL) return MLA_ERR_UNSUPPORTED;
+  if ((long long)B * Lmax + mla::kTok > 0x7fffffffLL) return MLA_ERR_UNSUPPORTED;
   const DeviceInfo* dev = device_info();
   if (!dev) return MLA_ERR_CUDA;
   const WsLayout w = ws_layout(B, S, H, dev->max_clusters);
@@ -450,17 +473,10 @@ extern "C" mla_status mla_decode_noalloc(const mla_bf16* q_cat, const mla_bf16* 
   mla::plan_kernel<<<1, 1024, 0, st>>>(pp);
   if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
 
-  CUtensorMap tc, tk;
-  const cuuint64_t cd[2] = {512, (cuuint64_t)B * Lmax};
-  const cuuint64_t cs[1] = {1024};
-  const cuuint32_t cb[2] = {64, 64};
-  const cuuint64_t kd[2] = {64, (cuuint64_t)B * Lmax};
-  const cuuint64_t ks[1] = {128};
-  if (!encode_tiled(&tc, c_kv, 2, cd, cs, cb) || !encode_tiled(&tk, k_r, 2, kd, ks, cb))
-    return MLA_ERR_INVALID_ARG;
+  DecodeMaps maps;
+  if (!encode_decode_maps(&maps, q_cat, c_kv, k_r, B, S, H, Lmax)) return MLA_ERR_INVALID_ARG;
 
   mla::DecodeParams p;
-  p.q_cat = reinterpret_cast<const __nv_bfloat16*>(q_cat);
   p.seqlens = seqlens;
   p.prefix = pp.prefix;
   p.gfirst = pp.gfirst;
@@ -491,9 +507,13 @@ extern "C" mla_status mla_decode_noalloc(const mla_bf16* q_cat, const mla_bf16* 
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, mla::decode_kernel, tc, tk, p) != cudaSuccess) return MLA_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, mla::decode_kernel, maps.c0, maps.kr, maps.q, maps.qr, maps.c1, p) !=
+      cudaSuccess)
+    return MLA_ERR_CUDA;
 
   mla::CombineParams cp;
+  cp.prefix = pp.prefix;
+  cp.gfirst = pp.gfirst;
   cp.segbase = pp.segbase;
   cp.ml = p.ml;
   cp.opart = p.opart;
@@ -503,6 +523,7 @@ extern "C" mla_status mla_decode_noalloc(const mla_bf16* q_cat, const mla_bf16* 
   cp.S = S;
   cp.H = H;
   cp.n_rb = w.n_rb;
+  cp.G = w.G;
   mla::combine_kernel<<<dim3((unsigned)(B * w.n_rb), 8), 128, 0, st>>>(cp);
   return launch_status();
 }

@@ -3,12 +3,13 @@
 // The softmax of "DeepSeek-V3" (ekkoxiao.github.io), "Multi-Head Latent
 // Attention / 注意力计算" normalises once over all visible positions.  The
 // decode kernel cuts every sequence's cache rows into contiguous runs of
-// 64-row tiles ("segments") spread over all SMs; each segment k leaves, per
+// 128-row tiles ("segments") spread over all SMs; each segment k leaves, per
 // query row, an unnormalised latent sum O_k = sum_j 2^(s2_j - m_k) c_j, its
 // reference exponent m_k (an integer, log2 units) and l_k = sum_j 2^(s2_j - m_k).
 // Merging them restores the single normalisation exactly:
 //     o_lat = sum_k 2^(m_k - M) O_k / sum_k 2^(m_k - M) l_k,   M = max_k m_k.
 //
+// Tiles are kTileRows = 128 cache rows (the N of the decode's QK^T MMAs).
 // Plan: the cache tiles of all sequences are laid end to end (sequence-major)
 // and cut into G equal runs, one per group of clusters.  Group g owns flat
 // tiles [floor(g T / G), floor((g+1) T / G)).  A sequence b contributes one
@@ -31,7 +32,9 @@ struct PlanParams {
   uint32_t* plan_ok;
 };
 
-__device__ __forceinline__ int tiles_of(int L) { return (L + 63) >> 6; }
+constexpr int kTileRows = 128;
+
+__device__ __forceinline__ int tiles_of(int L) { return (L + kTileRows - 1) / kTileRows; }
 
 // Group owning flat tile x: the largest g with floor(g T / G) <= x.
 __device__ __forceinline__ int group_of(int64_t x, int64_t T, int G) {
@@ -128,13 +131,23 @@ __global__ void __launch_bounds__(1024) plan_kernel(const PlanParams p) {
 }
 
 struct CombineParams {
+  const int32_t* prefix;   // plan: prefix[B] = total tiles T
+  const int32_t* gfirst;
   const int32_t* segbase;
   const float2* ml;     // [slots * n_rb, 128] (m_k, l_k)
   const float* opart;   // [slots * n_rb, 512, 128] column-major
   __nv_bfloat16* o_lat; // [B*S*H, 512]
   const uint32_t* plan_ok;
-  int B, S, H, n_rb;
+  int B, S, H, n_rb, G;
 };
+
+// Group g of G owns flat tiles [floor(g T / G), floor((g+1) T / G)); when
+// T < G some groups own none.  A sequence's segment slots cover every group
+// from its first to its last, so a slot of an empty group is never written
+// by the decode and must be skipped.
+__device__ __forceinline__ bool group_empty(int g, int64_t T, int G) {
+  return (int64_t)g * T / G == (int64_t)(g + 1) * T / G;
+}
 
 // Block = one 128-row block of one sequence and 64 latent columns; thread =
 // one query row.  Partials are column-major, so every load of a warp reads 32
@@ -146,10 +159,12 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
   const int SH = p.S * p.H;
   if (rb * 128 + r >= SH) return;
   if (*p.plan_ok == 0u) return;
-  const int k0 = p.segbase[b], k1 = p.segbase[b + 1];
+  const int k0 = p.segbase[b], k1 = p.segbase[b + 1], g0 = p.gfirst[b];
+  const int64_t T = p.prefix[p.B];
 
   float M = -INFINITY;
   for (int k = k0; k < k1; ++k) {
+    if (group_empty(g0 + k - k0, T, p.G)) continue;
     const float2 v = p.ml[((size_t)k * p.n_rb + rb) * 128 + r];
     if (v.y > 0.f) M = fmaxf(M, v.x);
   }
@@ -158,6 +173,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
   for (int i = 0; i < 64; ++i) acc[i] = 0.f;
   float den = 0.f;
   for (int k = k0; k < k1; ++k) {
+    if (group_empty(g0 + k - k0, T, p.G)) continue;
     const size_t idx = (size_t)k * p.n_rb + rb;
     const float2 v = p.ml[idx * 128 + r];
     if (!(v.y > 0.f)) continue;

@@ -194,6 +194,24 @@ def test_bad_seqlen_is_reported_and_recovers():
     assert_close(got, ref, what="after error")
 
 
+def test_decode_never_reads_unwritten_workspace():
+    # Few tiles and two row blocks: fewer tiles than split groups, so some
+    # groups own no tile.  The workspace (beyond its status word) is filled
+    # with finite garbage that a stray read would fold into the result.
+    q, c, k, sl = _latent_case(3, 2, 96, [2, 700, 2500], seed=202)
+    B, S, H = 3, 2, 96
+    ws = mb.new_workspace(B, S, H)
+    ws[256:] = 0x3F                     # every fp32 partial reads as 0.747
+    o = torch.empty(B, S, H, 512, dtype=torch.bfloat16, device="cuda")
+    for _ in range(2):
+        mb.decode(q.cuda(), c.cuda(), k.cuda(), sl.cuda(), ws)
+        mb.splitkv_combine(ws, o)
+        assert mb.read_status(ws) == mb.MLA_OK
+        ref = oracle.latent_attention(bits(q), bits(c), bits(k), sl.numpy(), d_r=64,
+                                      softmax_scale=1.0 / math.sqrt(192.0))
+        assert_close(f64(o), ref, what="garbage workspace")
+
+
 def test_workspace_too_small_is_rejected():
     q, c, k, sl = _latent_case(1, 1, 16, [10], seed=12)
     ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
