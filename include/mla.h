@@ -15,7 +15,8 @@
  *
  * One decode step is five calls on one stream:
  *   mla_absorb_q -> mla_rope_apply (queries) -> mla_decode
- *   -> mla_splitkv_combine -> mla_up_project.
+ *   -> mla_splitkv_combine -> mla_up_project,
+ * or four, with mla_absorb_rope_q doing the first two in one launch.
  * The cache's k^R is rotated once, when it is written (mla_rope_apply on the
  * cache), because the pages cache the rotated key.
  *
@@ -76,6 +77,19 @@ int mla_version(void);
  */
 mla_status mla_absorb_q(const mla_bf16 *q_nope, const mla_bf16 *W_UK, mla_bf16 *q_cat, int B,
                         int S, int H, void *stream);
+
+/*
+ * mla_absorb_q and the query RoPE in one launch: q_cat[..., 0:512] =
+ * (W_h^UK)^T q^C as mla_absorb_q, and q_cat[..., 512:576] = RoPE(q_rope) at
+ * position seqlens[b] - S + s as mla_rope_apply(MLA_POS_QUERY) ("Query": the
+ * decoupled query key q^R is rotated at the query's position).
+ *   q_rope  [B,S,H,64] bf16 (pre-RoPE),  seqlens [B] int32 device,
+ *   base    RoPE base (10000); other arguments as mla_absorb_q.
+ * Rows whose position seqlens[b] - S + s is negative keep their rope columns.
+ */
+mla_status mla_absorb_rope_q(const mla_bf16 *q_nope, const mla_bf16 *q_rope, const mla_bf16 *W_UK,
+                             const int32_t *seqlens, mla_bf16 *q_cat, int B, int S, int H,
+                             float base, void *stream);
 
 /* How mla_rope_apply finds the position of row n. */
 typedef enum {

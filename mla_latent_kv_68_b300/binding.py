@@ -52,6 +52,7 @@ def lib():
         L.mla_status_string.argtypes = [i32]
         L.mla_version.restype = i32
         L.mla_absorb_q.argtypes = [vp, vp, vp, i32, i32, i32, vp]
+        L.mla_absorb_rope_q.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, f32, vp]
         L.mla_rope_apply.argtypes = [vp, i64, i64, vp, i64, i64, i64, i32, i32, vp, i32, f32, vp]
         L.mla_decode_workspace_size.restype = sz
         L.mla_decode_workspace_size.argtypes = [i32, i32, i32]
@@ -60,8 +61,9 @@ def lib():
         L.mla_up_project.argtypes = [vp, vp, vp, i32, i32, i32, vp]
         L.mla_read_status.argtypes = [vp, vp]
         L.mla_decode_noalloc.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, f32, vp, vp]
-        for n in ("mla_absorb_q", "mla_rope_apply", "mla_decode", "mla_splitkv_combine",
-                  "mla_up_project", "mla_read_status", "mla_decode_noalloc"):
+        for n in ("mla_absorb_q", "mla_absorb_rope_q", "mla_rope_apply", "mla_decode",
+                  "mla_splitkv_combine", "mla_up_project", "mla_read_status",
+                  "mla_decode_noalloc"):
             getattr(L, n).restype = i32
         _lib = L
     return _lib
@@ -108,6 +110,20 @@ def absorb_q(q_nope, W_UK, q_cat, stream=None):
     _need(q_cat, "q_cat", shape=(B, S, H, D_QK))
     _check(lib().mla_absorb_q(_ptr(q_nope), _ptr(W_UK), _ptr(q_cat), B, S, H, _stream(stream)),
            "mla_absorb_q")
+
+
+def absorb_rope_q(q_nope, q_rope, W_UK, seqlens, q_cat, base=ROPE_BASE, stream=None):
+    """q_cat[..., :512] = W_UK[h]^T q_nope and q_cat[..., 512:] = RoPE(q_rope) at
+    positions seqlens[b] - S + s, in one launch."""
+    B, S, H, _ = q_nope.shape
+    _need(q_nope, "q_nope", shape=(B, S, H, D_H))
+    _need(q_rope, "q_rope", shape=(B, S, H, D_R))
+    _need(W_UK, "W_UK", shape=(H, D_H, D_C))
+    _need(seqlens, "seqlens", dtype=torch.int32, shape=(B,))
+    _need(q_cat, "q_cat", shape=(B, S, H, D_QK))
+    _check(lib().mla_absorb_rope_q(_ptr(q_nope), _ptr(q_rope), _ptr(W_UK), _ptr(seqlens),
+                                   _ptr(q_cat), B, S, H, base, _stream(stream)),
+           "mla_absorb_rope_q")
 
 
 def rope_apply(x_in, in_stride_n, in_stride_h, x_out, out_stride_n, out_stride_h, N, nh,
@@ -207,8 +223,8 @@ def read_status(workspace=None, stream=None) -> int:
 
 class DecodeStep:
     """Owns the per-step device buffers of one decode shape and issues the
-    five library calls of a step on one stream:
-    absorb -> RoPE(queries) -> decode -> combine -> up-project."""
+    four library calls of a step on one stream:
+    absorb + RoPE(queries) -> decode -> combine -> up-project."""
 
     def __init__(self, B: int, S: int, H: int, device="cuda"):
         self.B, self.S, self.H = B, S, H
@@ -226,8 +242,7 @@ class DecodeStep:
 
     # The three phases of a step, separately callable for per-phase timing.
     def queries(self, q_nope, q_rope, seqlens, W_UK, stream=None):
-        absorb_q(q_nope, W_UK, self.q_cat, stream)
-        rope_queries(q_rope, self.q_cat, seqlens, stream=stream)
+        absorb_rope_q(q_nope, q_rope, W_UK, seqlens, self.q_cat, stream=stream)
 
     def attend(self, c_kv, k_r, seqlens, softmax_scale=SOFTMAX_SCALE, stream=None):
         decode(self.q_cat, c_kv, k_r, seqlens, self.workspace, softmax_scale, stream)
@@ -247,4 +262,4 @@ class DecodeStep:
             fn(*args, **kwargs)
         return g
 
-    LAUNCHES_PER_STEP = 6  # absorb, rope, plan, decode, combine, up-projection
+    LAUNCHES_PER_STEP = 5  # absorb + rope, plan, decode, combine, up-projection

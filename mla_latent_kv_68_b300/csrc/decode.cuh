@@ -233,6 +233,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   __syncthreads();
   tc_fence_after();
   cluster_sync();  // the peer's barriers exist before anyone arrives on them remotely
+  pdl_trigger();
+  pdl_wait();      // q_cat and the plan come from the kernels before this one
   const uint32_t tmem = *tmem_slot;
   const bool run = (*p.plan_ok != 0u) && (*abort_flag == 0u);
 

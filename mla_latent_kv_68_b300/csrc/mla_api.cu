@@ -61,9 +61,9 @@ const DeviceInfo* device_info() {
       cudaFuncSetAttribute(mla::decode_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 0) !=
           cudaSuccess ||
       cudaFuncSetAttribute(mla::absorb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           32768 + 65536 + 64) != cudaSuccess ||
+                           (int)mla::absorb_smem_bytes(256)) != cudaSuccess ||
       cudaFuncSetAttribute(mla::up_project_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           8 * 16384 + 8 * 64 * 128 + 128) != cudaSuccess)
+                           (int)mla::up_smem_bytes(64)) != cudaSuccess)
     return nullptr;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -90,7 +90,7 @@ const DeviceInfo* device_info() {
 
 bool encode_tiled(CUtensorMap* map, const void* base, cuuint32_t rank, const cuuint64_t* dims,
                   const cuuint64_t* strides_bytes, const cuuint32_t* box) {
-  const cuuint32_t estr[3] = {1, 1, 1};
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
   return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims,
                   strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -155,6 +155,38 @@ mla_status launch_status() {
   return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
+// Launch with cudaLaunchKernelEx: optional 2-CTA cluster and optional
+// programmatic dependent launch (the kernel may start while the previous
+// kernel on the stream finishes; the kernels order themselves with
+// griddepcontrol.wait, see sm100.cuh).
+template <typename... KArgs, typename... Args>
+mla_status launch_ex(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                     cudaStream_t stream, bool pdl, int cluster_x, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  if (cluster_x > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster_x;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  if (pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  if (cudaLaunchKernelEx(&cfg, kernel, args...) != cudaSuccess) return MLA_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
 uint32_t pow2_at_least(uint32_t x) {
   uint32_t p = 32;
   while (p < x) p <<= 1;
@@ -180,8 +212,14 @@ const char* mla_status_string(int s) {
 
 int mla_version(void) { return 100; }
 
-mla_status mla_absorb_q(const mla_bf16* q_nope, const mla_bf16* W_UK, mla_bf16* q_cat, int B,
-                        int S, int H, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Shared body of mla_absorb_q and mla_absorb_rope_q (q_rope == nullptr: no RoPE).
+mla_status absorb_launch(const mla_bf16* q_nope, const mla_bf16* q_rope, const mla_bf16* W_UK,
+                         const int32_t* seqlens, mla_bf16* q_cat, int B, int S, int H, float base,
+                         void* stream) {
   if (!q_nope || !W_UK || !q_cat || !aligned16(q_nope) || !aligned16(W_UK) || !aligned16(q_cat))
     return MLA_ERR_INVALID_ARG;
   if (B < 1 || S < 1 || H < 1) return MLA_ERR_INVALID_ARG;
@@ -192,9 +230,10 @@ mla_status mla_absorb_q(const mla_bf16* q_nope, const mla_bf16* W_UK, mla_bf16* 
   if (!dev) return MLA_ERR_CUDA;
   const int n_tile = BS >= 256 ? 256 : (int)((BS + 15) / 16 * 16);
   CUtensorMap tw, tq;
-  const cuuint64_t wd[3] = {512, 128, (cuuint64_t)H};
-  const cuuint64_t ws[2] = {1024, 128 * 1024};
-  const cuuint32_t wb[3] = {64, 128, 1};
+  // W_UK [H*128 d-rows][512 k] seen as [64 k][H*128 rows][8 k-blocks]: one box = 2 atoms
+  const cuuint64_t wd[3] = {64, (cuuint64_t)H * 128, 8};
+  const cuuint64_t ws[2] = {1024, 128};
+  const cuuint32_t wb[3] = {64, 128, 2};
   const cuuint64_t qd[3] = {128, (cuuint64_t)H, (cuuint64_t)BS};
   const cuuint64_t qs[2] = {256, (cuuint64_t)H * 256};
   const cuuint32_t qb[3] = {64, 1, (cuuint32_t)n_tile};
@@ -202,16 +241,38 @@ mla_status mla_absorb_q(const mla_bf16* q_nope, const mla_bf16* W_UK, mla_bf16* 
     return MLA_ERR_INVALID_ARG;
   mla::AbsorbParams p;
   p.q_cat = reinterpret_cast<__nv_bfloat16*>(q_cat);
+  p.q_rope = reinterpret_cast<const __nv_bfloat16*>(q_rope);
+  p.seqlens = seqlens;
   p.BS = (int)BS;
+  p.S = S;
   p.H = H;
   p.n_tile = n_tile;
-  p.tmem_cols = pow2_at_least((uint32_t)n_tile);
+  p.tmem_cols = pow2_at_least((uint32_t)(2 * n_tile));
   p.status = dev->kernel_status;
   p.timeout_ns = kTimeoutNs;
-  const dim3 grid(H, 4, (unsigned)((BS + n_tile - 1) / n_tile));
-  const size_t smem = 32768 + (size_t)n_tile * 256 + 64;
-  mla::absorb_kernel<<<grid, mla::kAbsorbThreads, smem, (cudaStream_t)stream>>>(tw, tq, p);
+  mla::RopeTheta th;
+  for (int j = 0; j < 32; ++j) th.theta[j] = std::pow((double)base, -2.0 * j / 64.0);
+  const dim3 grid(H, 2, (unsigned)((BS + n_tile - 1) / n_tile));
+  mla::absorb_kernel<<<grid, mla::kAbsorbThreads, mla::absorb_smem_bytes(n_tile),
+                       (cudaStream_t)stream>>>(tw, tq, p, th);
   return launch_status();
+}
+
+}  // namespace
+
+extern "C" {
+
+mla_status mla_absorb_q(const mla_bf16* q_nope, const mla_bf16* W_UK, mla_bf16* q_cat, int B,
+                        int S, int H, void* stream) {
+  return absorb_launch(q_nope, nullptr, W_UK, nullptr, q_cat, B, S, H, 10000.0f, stream);
+}
+
+mla_status mla_absorb_rope_q(const mla_bf16* q_nope, const mla_bf16* q_rope, const mla_bf16* W_UK,
+                             const int32_t* seqlens, mla_bf16* q_cat, int B, int S, int H,
+                             float base, void* stream) {
+  if (!q_rope || !seqlens || !aligned16(q_rope)) return MLA_ERR_INVALID_ARG;
+  if (!(base > 1.0f) || !std::isfinite(base)) return MLA_ERR_INVALID_ARG;
+  return absorb_launch(q_nope, q_rope, W_UK, seqlens, q_cat, B, S, H, base, stream);
 }
 
 mla_status mla_rope_apply(const mla_bf16* x_in, int64_t in_stride_n, int64_t in_stride_h,
@@ -277,8 +338,8 @@ mla_status mla_decode(const mla_bf16* q_cat, const mla_bf16* c_kv, const mla_bf1
   pp.gstart = reinterpret_cast<int32_t*>(ws + w.gstart);
   pp.status = reinterpret_cast<uint32_t*>(ws);
   pp.plan_ok = reinterpret_cast<uint32_t*>(ws) + 1;
-  mla::plan_kernel<<<1, 1024, 0, st>>>(pp);
-  if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
+  const mla_status ps = launch_ex(mla::plan_kernel, dim3(1), dim3(1024), 0, st, true, 1, pp);
+  if (ps != MLA_OK) return ps;
 
   DecodeMaps maps;
   if (!encode_decode_maps(&maps, q_cat, c_kv, k_r, B, S, H, Lmax)) return MLA_ERR_INVALID_ARG;
@@ -302,23 +363,10 @@ mla_status mla_decode(const mla_bf16* q_cat, const mla_bf16* c_kv, const mla_bf1
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
   p.timeout_ns = kTimeoutNs;
 
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.gridDim = dim3(2 * w.G * w.n_rb);
-  cfg.blockDim = dim3(mla::kDecThreads);
-  cfg.dynamicSmemBytes = mla::kDecSmem;
-  cfg.stream = st;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, mla::decode_kernel, maps.c0, maps.kr, maps.q, maps.qr, maps.c1, p) !=
-      cudaSuccess)
-    return MLA_ERR_CUDA;
-  return launch_status();
+  return launch_ex(mla::decode_kernel, dim3(2 * w.G * w.n_rb), dim3(mla::kDecThreads), mla::kDecSmem,
+                   st, true, 2, maps.c0, maps.kr, maps.q, maps.qr, maps.c1, p);
 }
+
 
 mla_status mla_splitkv_combine(const void* workspace, size_t workspace_bytes, mla_bf16* o_lat,
                                int B, int S, int H, void* stream) {
@@ -344,9 +392,8 @@ mla_status mla_splitkv_combine(const void* workspace, size_t workspace_bytes, ml
   p.H = H;
   p.n_rb = w.n_rb;
   p.G = w.G;
-  const dim3 grid((unsigned)(B * w.n_rb), 8);
-  mla::combine_kernel<<<grid, 128, 0, (cudaStream_t)stream>>>(p);
-  return launch_status();
+  const dim3 grid((unsigned)(B * w.n_rb), 512 / mla::kCombineCols);
+  return launch_ex(mla::combine_kernel, grid, dim3(128), 0, (cudaStream_t)stream, true, 1, p);
 }
 
 mla_status mla_up_project(const mla_bf16* o_lat, const mla_bf16* W_UV, mla_bf16* out, int B,
@@ -361,13 +408,15 @@ mla_status mla_up_project(const mla_bf16* o_lat, const mla_bf16* W_UV, mla_bf16*
   if (!dev) return MLA_ERR_CUDA;
   const int n_tile = BS >= 64 ? 64 : (int)((BS + 15) / 16 * 16);
   CUtensorMap tw, to;
-  const cuuint64_t wd[3] = {512, 128, (cuuint64_t)H};
-  const cuuint64_t ws[2] = {1024, 128 * 1024};
-  const cuuint32_t wb[3] = {64, 128, 1};
-  const cuuint64_t od[3] = {512, (cuuint64_t)H, (cuuint64_t)BS};
-  const cuuint64_t os[2] = {1024, (cuuint64_t)H * 1024};
-  const cuuint32_t ob[3] = {64, 1, (cuuint32_t)n_tile};
-  if (!encode_tiled(&tw, W_UV, 3, wd, ws, wb) || !encode_tiled(&to, o_lat, 3, od, os, ob))
+  // W_UV [H*128 v-rows][512 k] seen as [64 k][H*128 rows][8 k-blocks]: one box = 2 atoms
+  const cuuint64_t wd[3] = {64, (cuuint64_t)H * 128, 8};
+  const cuuint64_t ws[2] = {1024, 128};
+  const cuuint32_t wb[3] = {64, 128, 2};
+  // o_lat [BS][H][512] seen as [64 k][BS][8 k-blocks][H]: one box = all 8 atoms of n_tile rows
+  const cuuint64_t od[4] = {64, (cuuint64_t)BS, 8, (cuuint64_t)H};
+  const cuuint64_t os[3] = {(cuuint64_t)H * 1024, 128, 1024};
+  const cuuint32_t ob[4] = {64, (cuuint32_t)n_tile, 8, 1};
+  if (!encode_tiled(&tw, W_UV, 3, wd, ws, wb) || !encode_tiled(&to, o_lat, 4, od, os, ob))
     return MLA_ERR_INVALID_ARG;
   mla::UpParams p;
   p.out = reinterpret_cast<__nv_bfloat16*>(out);
@@ -378,9 +427,8 @@ mla_status mla_up_project(const mla_bf16* o_lat, const mla_bf16* W_UV, mla_bf16*
   p.status = dev->kernel_status;
   p.timeout_ns = kTimeoutNs;
   const dim3 grid(H, (unsigned)((BS + n_tile - 1) / n_tile));
-  const size_t smem = 8 * 16384 + (size_t)8 * n_tile * 128 + 128;
-  mla::up_project_kernel<<<grid, mla::kUpThreads, smem, (cudaStream_t)stream>>>(tw, to, p);
-  return launch_status();
+  return launch_ex(mla::up_project_kernel, grid, dim3(mla::kUpThreads), mla::up_smem_bytes(n_tile),
+                   (cudaStream_t)stream, true, 1, tw, to, p);
 }
 
 mla_status mla_read_status(void* workspace, void* stream) {
@@ -524,6 +572,6 @@ extern "C" mla_status mla_decode_noalloc(const mla_bf16* q_cat, const mla_bf16* 
   cp.H = H;
   cp.n_rb = w.n_rb;
   cp.G = w.G;
-  mla::combine_kernel<<<dim3((unsigned)(B * w.n_rb), 8), 128, 0, st>>>(cp);
+  mla::combine_kernel<<<dim3((unsigned)(B * w.n_rb), 512 / mla::kCombineCols), 128, 0, st>>>(cp);
   return launch_status();
 }

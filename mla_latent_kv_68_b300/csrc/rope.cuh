@@ -24,6 +24,30 @@ struct RopeTheta {
 
 enum : int { kPosExplicit = 0, kPosQuery = 1, kPosCache = 2 };
 
+// Rotate the 4 interleaved pairs (16 bytes) at pairs part*4 .. part*4+3 of a
+// 64-element row sitting at position `pos`.
+__device__ __forceinline__ uint4 rope_rotate4(uint4 v, int64_t pos, int part, const RopeTheta& th) {
+  uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  const double two_pi = 6.283185307179586476925286766559;
+  const double inv_two_pi = 0.15915494309189533576888376337251;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int j = part * 4 + k;
+    const double a = (double)pos * th.theta[j];
+    const double r = fma(-rint(a * inv_two_pi), two_pi, a);
+    float sn, cs;
+    sincosf((float)r, &sn, &cs);
+    __nv_bfloat162 pr = *reinterpret_cast<__nv_bfloat162*>(&w[k]);
+    const float x = __low2float(pr), y = __high2float(pr);
+    const float xo = x * cs - y * sn;
+    const float yo = x * sn + y * cs;
+    __nv_bfloat162 o = __floats2bfloat162_rn(xo, yo);
+    w[k] = *reinterpret_cast<uint32_t*>(&o);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+
 __global__ void __launch_bounds__(256) rope_kernel(const __nv_bfloat16* __restrict__ x_in,
                                                    int64_t in_sn, int64_t in_sh,
                                                    __nv_bfloat16* __restrict__ x_out,
@@ -55,25 +79,7 @@ __global__ void __launch_bounds__(256) rope_kernel(const __nv_bfloat16* __restri
   }
 
   const uint4 v = *reinterpret_cast<const uint4*>(x_in + n * in_sn + hd * in_sh + part * 8);
-  uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  const double two_pi = 6.283185307179586476925286766559;
-  const double inv_two_pi = 0.15915494309189533576888376337251;
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int j = part * 4 + k;
-    const double a = (double)pos * th.theta[j];
-    const double r = fma(-rint(a * inv_two_pi), two_pi, a);
-    float sn, cs;
-    sincosf((float)r, &sn, &cs);
-    __nv_bfloat162 pr = *reinterpret_cast<__nv_bfloat162*>(&w[k]);
-    const float x = __low2float(pr), y = __high2float(pr);
-    const float xo = x * cs - y * sn;
-    const float yo = x * sn + y * cs;
-    __nv_bfloat162 o = __floats2bfloat162_rn(xo, yo);
-    w[k] = *reinterpret_cast<uint32_t*>(&o);
-  }
-  *reinterpret_cast<uint4*>(x_out + n * out_sn + hd * out_sh + part * 8) =
-      make_uint4(w[0], w[1], w[2], w[3]);
+  *reinterpret_cast<uint4*>(x_out + n * out_sn + hd * out_sh + part * 8) = rope_rotate4(v, pos, part, th);
 }
 
 }  // namespace mla

@@ -73,6 +73,8 @@ __device__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
 __global__ void __launch_bounds__(1024) plan_kernel(const PlanParams p) {
   __shared__ int warp_sums[33];
   __shared__ int bad;
+  pdl_trigger();
+  pdl_wait();  // the workspace may still be read by the previous step's kernels
   const int nt = blockDim.x;
   if (threadIdx.x == 0) bad = 0;
   __syncthreads();
@@ -149,15 +151,21 @@ __device__ __forceinline__ bool group_empty(int g, int64_t T, int G) {
   return (int64_t)g * T / G == (int64_t)(g + 1) * T / G;
 }
 
-// Block = one 128-row block of one sequence and 64 latent columns; thread =
-// one query row.  Partials are column-major, so every load of a warp reads 32
-// consecutive floats.
+// Block = one 128-row block of one sequence and kCombineCols latent columns;
+// thread = one query row.  Partials are column-major, so every load of a warp
+// reads 32 consecutive floats.  The (m, l) of all segments are read first;
+// the partial columns of two segments are then loaded together so that the
+// few L2 round trips of a row overlap.
+constexpr int kCombineCols = 32;
+
 __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
+  pdl_trigger();
+  pdl_wait();  // the partials come from the decode kernel
   const int b = blockIdx.x / p.n_rb, rb = blockIdx.x - b * p.n_rb;
-  const int c0 = blockIdx.y * 64;
+  const int c0 = blockIdx.y * kCombineCols;
   const int r = threadIdx.x;
   const int SH = p.S * p.H;
-  if (rb * 128 + r >= SH) return;
+  if (c0 >= 512 || rb * 128 + r >= SH) return;
   if (*p.plan_ok == 0u) return;
   const int k0 = p.segbase[b], k1 = p.segbase[b + 1], g0 = p.gfirst[b];
   const int64_t T = p.prefix[p.B];
@@ -168,25 +176,40 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
     const float2 v = p.ml[((size_t)k * p.n_rb + rb) * 128 + r];
     if (v.y > 0.f) M = fmaxf(M, v.x);
   }
-  float acc[64];
+  float acc[kCombineCols];
 #pragma unroll
-  for (int i = 0; i < 64; ++i) acc[i] = 0.f;
+  for (int i = 0; i < kCombineCols; ++i) acc[i] = 0.f;
   float den = 0.f;
-  for (int k = k0; k < k1; ++k) {
-    if (group_empty(g0 + k - k0, T, p.G)) continue;
-    const size_t idx = (size_t)k * p.n_rb + rb;
-    const float2 v = p.ml[idx * 128 + r];
-    if (!(v.y > 0.f)) continue;
-    const float w = exp2f(v.x - M);
-    den += w * v.y;
-    const float* src = p.opart + (idx * 512 + c0) * 128 + r;
+  for (int k = k0; k < k1; k += 2) {
+    float w[2];
+    const float* src[2];
 #pragma unroll
-    for (int c = 0; c < 64; ++c) acc[c] += w * __ldg(src + (size_t)c * 128);
+    for (int u = 0; u < 2; ++u) {
+      const int kk = k + u;
+      w[u] = 0.f;
+      src[u] = p.opart;
+      if (kk < k1 && !group_empty(g0 + kk - k0, T, p.G)) {
+        const size_t idx = (size_t)kk * p.n_rb + rb;
+        const float2 v = p.ml[idx * 128 + r];
+        if (v.y > 0.f) {
+          w[u] = exp2f(v.x - M);
+          den += w[u] * v.y;
+          src[u] = p.opart + (idx * 512 + c0) * 128 + r;
+        }
+      }
+    }
+    float x[2][kCombineCols];
+#pragma unroll
+    for (int u = 0; u < 2; ++u)
+#pragma unroll
+      for (int c = 0; c < kCombineCols; ++c) x[u][c] = w[u] != 0.f ? __ldg(src[u] + (size_t)c * 128) : 0.f;
+#pragma unroll
+    for (int c = 0; c < kCombineCols; ++c) acc[c] += w[0] * x[0][c] + w[1] * x[1][c];
   }
   const float inv = den > 0.f ? 1.f / den : 0.f;
   uint4* dst = reinterpret_cast<uint4*>(p.o_lat + ((size_t)b * SH + rb * 128 + r) * 512 + c0);
 #pragma unroll
-  for (int q = 0; q < 8; ++q)
+  for (int q = 0; q < kCombineCols / 8; ++q)
     dst[q] = make_uint4(pack_bf16x2(acc[8 * q] * inv, acc[8 * q + 1] * inv),
                         pack_bf16x2(acc[8 * q + 2] * inv, acc[8 * q + 3] * inv),
                         pack_bf16x2(acc[8 * q + 4] * inv, acc[8 * q + 5] * inv),

@@ -103,6 +103,24 @@ def test_absorb_matches_oracle(B, S, H):
     assert rel_l2(g64, ref) < 3e-3
 
 
+@pytest.mark.parametrize("B,S,H", [(1, 1, 16), (32, 1, 128), (16, 2, 128), (3, 2, 5), (300, 1, 2)])
+def test_absorb_rope_matches_oracle(B, S, H):
+    g = torch.Generator().manual_seed(B * 977 + S * 31 + H)
+    q = torch.randn(B, S, H, 128, generator=g).to(torch.bfloat16)
+    qr = torch.randn(B, S, H, 64, generator=g).to(torch.bfloat16)
+    W = (torch.randn(H, 128, 512, generator=g) / math.sqrt(512)).to(torch.bfloat16)
+    seqlens = torch.randint(S, 140000, (B,), generator=g, dtype=torch.int32)
+    seqlens[0] = S                                   # the query at position 0 .. S-1
+    q_cat = torch.full((B, S, H, 576), float("nan"), dtype=torch.bfloat16, device="cuda")
+    mb.absorb_rope_q(q.cuda(), qr.cuda(), W.cuda(), seqlens.cuda(), q_cat)
+    got = q_cat.cpu().double().numpy()
+    ref = oracle.absorb(bits(q).reshape(B * S, H, 128), bits(W)).reshape(B, S, H, 512)
+    assert (np.abs(got[..., :512] - ref) <= 2.0 ** -8 * np.abs(ref) + 2e-4).all()
+    pos = np.array([[L - S + s for s in range(S)] for L in seqlens.tolist()]).reshape(-1)
+    rref = oracle.rope(bits(qr).reshape(-1, 64), np.repeat(pos, H)).reshape(B, S, H, 64)
+    assert (np.abs(got[..., 512:] - rref) <= 2.0 ** -8 * np.abs(rref) + 1e-5).all()
+
+
 @pytest.mark.parametrize("B,S,H", [(1, 1, 16), (32, 1, 128), (64, 1, 128), (100, 1, 3),
                                    (16, 2, 128)])
 def test_up_project_matches_oracle(B, S, H):
