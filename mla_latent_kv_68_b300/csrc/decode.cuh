@@ -14,10 +14,11 @@
 // from N = 128 up (N = 64 reaches about half of it), so both contractions use
 // N >= 128.  The fp32 accumulator O (128 x 512) fills one SM's whole tensor
 // memory, so each unit of work is a CLUSTER OF TWO CTAs on two SMs:
-//   rank 0 ("score CTA"): q~ (128 x 512 bf16) lives in its tensor memory as
-//       the A operand of the QK^T MMAs (A-from-TMEM form), q^R (128 x 64) in
-//       shared memory; two 128-column S buffers complete the 512 columns.
-//       Every operand arrives through one ring of 32 KB stages, each one TMA
+//   rank 0 ("score CTA"): q~ (128 x 512 bf16) and q^R (128 x 64) live in its
+//       tensor memory as the A operand of the QK^T MMAs (A-from-TMEM form),
+//       next to one 128-column S buffer; shared memory is left to the TMA
+//       ring, whose depth sets how many bytes an SM keeps in flight.
+//       Every operand arrives through a 6-stage ring of 32 KB stages, each one TMA
 //       box of two 128-row x 64-column blocks (one 128-byte-swizzle atom per
 //       block): a tile is 5 stages (4 of c, 1 of k^R), and at a segment start
 //       the 128 query rows of q_cat pass through the same ring (5 stages) on
@@ -27,7 +28,7 @@
 //       Eight softmax
 //       warps (two threads per query row, 64 tokens each) run the online
 //       softmax, write P (bf16, in the swizzled K-major layout the MMA reads)
-//       and the per-row rescale factor into a local staging buffer, and one
+//       and the per-row rescale exponent into a local staging buffer, and one
 //       thread moves it into rank 1 with a single bulk shared-to-shared copy
 //       that completes a transaction-counted barrier there.
 //   rank 1 ("value CTA"): O lives in all 512 columns of its tensor memory; it
@@ -65,13 +66,13 @@ constexpr int kTok = kTileRows;   // cache rows per tile (128)
 // score CTA (rank 0)
 constexpr int kBlk0 = kTok * 128;          // one block: 128 rows x 64 bf16 = 16 KB
 constexpr int kStage0 = 2 * kBlk0;         // one stage: two blocks (one TMA box)
-constexpr int kStages0 = 5;
+constexpr int kStages0 = 6;
 constexpr int kStagesPerTile = 5;          // c: 4 stages, k^R: 1 (q_cat: 4 + 1 for q^R)
-constexpr int kOffQR = kStages0 * kStage0; // q^R: 128 rows x 64 bf16, 128-byte swizzle
-constexpr int kOffPS = kOffQR + 16384;     // P staging: 128 x 128 bf16 + alpha[128]
+constexpr int kOffPS = kStages0 * kStage0; // P staging: 128 x 128 bf16 + rescale exponents[128]
 constexpr int kPBytes = 128 * kTok * 2;
-constexpr uint32_t kPTx = kPBytes + 128 * 4;  // bytes of one P slot with its alpha column
-constexpr int kOffXch = kOffPS + (int)kPTx;   // row max [2 tiles][2 halves][128], row sum [2][128]
+constexpr uint32_t kPTx = kPBytes + 128;      // bytes of one P slot with its exponent column
+constexpr int kOffXch = kOffPS + (int)kPTx;   // ceil(row max) int16 [2 tiles][2 halves][128], row sum f32 [128]
+constexpr int kXchBytes = 2 * 2 * 128 * 2 + 128 * 4;
 // value CTA (rank 1)
 constexpr int kSub = 32;                   // cache rows per value-CTA stage
 constexpr int kBlk1 = kSub * 128;          // 4 KB
@@ -80,22 +81,23 @@ constexpr int kStages1 = 4;
 constexpr int kOffP = kStages1 * kStage1;  // P slots [2], each P then alpha
 constexpr int kPSlot = 33 * 1024;          // slot stride (keeps P 1 KB aligned)
 // shared by both
-constexpr int kEnd0 = kOffXch + 3072, kEnd1 = kOffP + 2 * kPSlot;
+constexpr int kEnd0 = kOffXch + kXchBytes, kEnd1 = kOffP + 2 * kPSlot;
 constexpr int kOffBar = kEnd0 > kEnd1 ? kEnd0 : kEnd1;
 constexpr int kNumBars = 46;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kDecSmem = kOffMisc + 16;
 static_assert(kDecSmem <= 232448, "decode shared memory exceeds 227 KB");
-static_assert(kOffQR % 1024 == 0 && kOffPS % 1024 == 0 && kOffP % 1024 == 0 && kPSlot % 1024 == 0,
+static_assert(kOffPS % 1024 == 0 && kOffP % 1024 == 0 && kPSlot % 1024 == 0,
               "swizzled operands need 1 KB alignment");
-static_assert(kPTx == (uint32_t)kPBytes + 512 && kPTx % 16 == 0 && kPTx <= (uint32_t)kPSlot,
+static_assert(kPTx % 16 == 0 && kPTx <= (uint32_t)kPSlot,
               "P slot layout");
-constexpr uint32_t kQCol = 256;  // score CTA: q~ at tensor-memory columns 256..511
+constexpr uint32_t kQCol = 256;   // score CTA: q~ at tensor-memory columns 256..511
+constexpr uint32_t kQRCol = 128;  // score CTA: q^R at columns 128..159; S at 0..127
 
 // barrier indices
 enum : int {
   B_FULL = 0, B_EMPTY = 10,          // TMA ring (rank 0: 5 stages, rank 1: 4)
-  B_SFULL = 20, B_SEMPTY = 22,       // score CTA: S buffers
+  B_SFULL = 20, B_SEMPTY = 22,       // score CTA: S buffer (one; index 0 used)
   B_PEMPTY = 24,                     // score CTA: P slot in the value CTA free again
   B_QREADY = 26,                     // score CTA: Q of the segment is in place
   B_XCH = 27,                        // score CTA: row-max exchange [tile parity][quadrant]
@@ -288,17 +290,15 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     if (lane == 0) {
       if (rank == 0) {
         constexpr uint32_t idesc = idesc_bf16_f32(128, kTok, 0, 0);
-        const uint32_t qr = smem_u32(smem + kOffQR);
         for_each_tile(p, g, [&](const TileInfo& ti) {
-          const int slot = ti.i & 1;
-          const uint32_t sph = (uint32_t)(ti.i >> 1) & 1u;
+          const uint32_t sph = (uint32_t)ti.i & 1u;  // the single S buffer, one phase per tile
           if (ti.first) {  // the query stages have been moved out of the ring: release them
             if (!mbar_wait(&bar[B_QREADY], (uint32_t)ti.k & 1u, wc)) return false;
             for (int j = 0; j < kStagesPerTile; ++j)
               mbar_arrive(&bar[B_EMPTY + ring_q_stage(ti.i, ti.k, j) % kStages0]);
           }
-          if (!mbar_wait(&bar[B_SEMPTY + slot], sph ^ 1u, wc)) return false;
-          const uint32_t d = tmem + (uint32_t)slot * kTok;
+          if (!mbar_wait(&bar[B_SEMPTY], sph ^ 1u, wc)) return false;
+          const uint32_t d = tmem;
           for (int j = 0; j < kStagesPerTile; ++j) {
             const int q = ring_kv_stage(ti.i, ti.k, j), st = q % kStages0;
             if (!mbar_wait(&bar[B_FULL + st], (uint32_t)(q / kStages0) & 1u, wc)) return false;
@@ -313,13 +313,12 @@ __global__ void __launch_bounds__(kDecThreads, 1)
               }
             } else {
 #pragma unroll
-              for (int kk = 0; kk < 4; ++kk)  // k^R against q^R from shared memory
-                mma_ss(d, smem_desc(qr + kk * 32, 16, 1024, 2), smem_desc(sbase + kk * 32, 16, 1024, 2),
-                       idesc, 1u);
+              for (int kk = 0; kk < 4; ++kk)  // k^R against q^R, both 64 wide
+                mma_ts(d, tmem + kQRCol + (uint32_t)kk * 8, smem_desc(sbase + kk * 32, 16, 1024, 2), idesc, 1u);
             }
             mma_commit(&bar[B_EMPTY + st]);
           }
-          mma_commit(&bar[B_SFULL + slot]);
+          mma_commit(&bar[B_SFULL]);
           return true;
         });
       } else {
@@ -397,7 +396,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 
     if (rank == 0) {
       // ---------------------------------------- scores + online softmax
-      float* xch = reinterpret_cast<float*>(smem + kOffXch);  // [2][2][128], then l [2][128]
+      int16_t* xch = reinterpret_cast<int16_t*>(smem + kOffXch);          // [2][2][128]
+      float* xl = reinterpret_cast<float*>(smem + kOffXch + 2 * 2 * 128 * 2);  // [128]
       uint8_t* ps = smem + kOffPS;
       float m_ref = -INFINITY, l = 0.f;
       int limit = 0;
@@ -418,12 +418,14 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                 v[4 * ch] = x.x; v[4 * ch + 1] = x.y; v[4 * ch + 2] = x.z; v[4 * ch + 3] = x.w;
               }
               tmem_st32(tl + kQCol + (uint32_t)j * 32, v);
-            } else {  // q^R keeps the same swizzled row layout
+            } else {  // q^R: 32 tensor-memory columns
+              uint32_t v[32];
 #pragma unroll
-              for (int ch = 0; ch < 8; ++ch)
-                *reinterpret_cast<uint4*>(smem + kOffQR + r * 128 + ch * 16) =
-                    *reinterpret_cast<const uint4*>(rowp + ch * 16);
-              fence_proxy_async_cta();
+              for (int ch = 0; ch < 8; ++ch) {
+                const uint4 x = *reinterpret_cast<const uint4*>(rowp + ((ch ^ (r & 7)) << 4));
+                v[4 * ch] = x.x; v[4 * ch + 1] = x.y; v[4 * ch + 2] = x.z; v[4 * ch + 3] = x.w;
+              }
+              tmem_st32(tl + kQRCol, v);
             }
           }
           tmem_wait_st();
@@ -434,18 +436,18 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         }
         const int slot = ti.i & 1;
         const uint32_t sph = (uint32_t)(ti.i >> 1) & 1u;
-        if (!warp_wait(&bar[B_SFULL + slot], sph, wc)) return false;
+        if (!warp_wait(&bar[B_SFULL], (uint32_t)ti.i & 1u, wc)) return false;
         tc_fence_after();
         uint32_t sv[64];
         {
           uint32_t (&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[0]);
           uint32_t (&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[32]);
-          tmem_ld32(tl + (uint32_t)(slot * kTok + hf * 64), lo);
-          tmem_ld32(tl + (uint32_t)(slot * kTok + hf * 64 + 32), hi);
+          tmem_ld32(tl + (uint32_t)(hf * 64), lo);
+          tmem_ld32(tl + (uint32_t)(hf * 64 + 32), hi);
         }
         tmem_wait_ld();
         tc_fence_before();
-        mbar_arrive(&bar[B_SEMPTY + slot]);
+        mbar_arrive(&bar[B_SEMPTY]);
 
         const int nv = min(max(limit - ti.t * kTok - hf * 64, 0), 64);
         float mx = -INFINITY;  // max of the raw scores; the scale is positive
@@ -453,16 +455,20 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         for (int c = 0; c < 64; ++c)
           if (c < nv) mx = fmaxf(mx, __uint_as_float(sv[c]));
         mx *= p.scale_log2;
-        // both threads of the row (same quadrant, warps q4 and q4 + 4) take the same maximum
-        xch[(slot * 2 + hf) * 128 + r] = mx;
+        // Both threads of the row (same quadrant, warps q4 and q4 + 4) need the
+        // same new reference exponent, which depends on the row maximum only
+        // through ceil(max): for an integer m, max > m + 8 iff ceil(max) > m + 8.
+        // So the two halves exchange ceil(max) as a 16-bit integer.
+        const int cm = mx == -INFINITY ? -32768 : (int)fminf(fmaxf(ceilf(mx), -32000.f), 32000.f);
+        xch[(slot * 2 + hf) * 128 + r] = (int16_t)cm;
         mbar_arrive(&bar[B_XCH + slot * 4 + q4]);
         if (!warp_wait(&bar[B_XCH + slot * 4 + q4], sph, wc)) return false;
-        mx = fmaxf(mx, xch[(slot * 2 + (hf ^ 1)) * 128 + r]);
-        float alpha = 1.f;
-        if (mx > m_ref + 8.f) {
-          const float mn = ceilf(mx);
-          alpha = (m_ref == -INFINITY) ? 0.f : exp2_int((int)(m_ref - mn));
-          l *= alpha;
+        const int cmax = max(cm, (int)xch[(slot * 2 + (hf ^ 1)) * 128 + r]);
+        int ex = 0;  // rescale 2^-ex of O and l; 255 stands for 0
+        if (cmax > -32768 && (float)cmax > m_ref + 8.f) {
+          const float mn = (float)cmax;
+          ex = (m_ref == -INFINITY) ? 255 : min((int)(mn - m_ref), 255);
+          l = (ex == 255) ? 0.f : l * exp2_int(-ex);
           m_ref = mn;
         }
         const float mu = (m_ref == -INFINITY) ? 0.f : m_ref;
@@ -487,16 +493,15 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         for (int ch = 0; ch < 8; ++ch)  // 128-byte swizzle: chunk ch of row r sits at ch ^ (r & 7)
           *reinterpret_cast<uint4*>(row + ((ch ^ (r & 7)) << 4)) =
               make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-        if (hf == 0) reinterpret_cast<float*>(ps + kPBytes)[r] = alpha;
+        if (hf == 0) ps[kPBytes + r] = (uint8_t)ex;
         fence_proxy_async_cta();  // the bulk copy reads the buffer through the async proxy
         mbar_arrive(&bar[B_PSTAGED]);
         if (ti.last) {  // segment end: add the two halves' sums, write (m, l)
-          float* xl = xch + 512;  // [2][128]
-          xl[hf * 128 + r] = l;
+          if (hf == 1) xl[r] = l;
           mbar_arrive(&bar[B_XL]);
           if (!warp_wait(&bar[B_XL], (uint32_t)ti.k & 1u, wc)) return false;
           if (hf == 0 && valid)
-            p.ml[((size_t)ti.slot * p.n_rb + rb) * 128 + r] = make_float2(mu, l + xl[128 + r]);
+            p.ml[((size_t)ti.slot * p.n_rb + rb) * 128 + r] = make_float2(mu, l + xl[r]);
           // the next segment's exchange reuses xl only after its own tiles'
           // row-max exchanges, which both threads pass after reading it here
         }
@@ -513,8 +518,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         const int q0 = q;
         q += nsub;
         if (!warp_wait(&bar[B_PFULL + slot], sph, wc)) return false;
-        const float alpha =
-            reinterpret_cast<const volatile float*>(smem + kOffP + slot * kPSlot + kPBytes)[r];
+        const int ex = reinterpret_cast<const volatile uint8_t*>(smem + kOffP + slot * kPSlot + kPBytes)[r];
+        const float alpha = ex == 255 ? 0.f : exp2_int(-ex);
         if (wt == 0) mbar_arrive_expect_tx(&bar[B_PFULL + slot], kPTx);  // arm the slot's next phase
         const bool need = !ti.first && alpha != 1.f;
         if (__any_sync(0xffffffffu, need)) {
