@@ -32,8 +32,8 @@
 //       thread moves it into rank 1 with a single bulk shared-to-shared copy
 //       that completes a transaction-counted barrier there.
 //   rank 1 ("value CTA"): O lives in all 512 columns of its tensor memory; it
-//       streams the 512-wide c rows of the same tiles in 32-token stages (one
-//       32 KB box each; L2 hits right after rank 0's reads, so HBM sees every
+//       streams the 512-wide c rows of the same tiles in 64-token stages (one
+//       64 KB box each; L2 hits right after rank 0's reads, so HBM sees every
 //       cache byte once) and issues O += P . C with N = 256 and C read as an
 //       MN-major operand straight from the TMA tile.
 // Neither CTA duplicates the other's tensor work.
@@ -74,10 +74,11 @@ constexpr uint32_t kPTx = kPBytes + 128;      // bytes of one P slot with its ex
 constexpr int kOffXch = kOffPS + (int)kPTx;   // ceil(row max) int16 [2 tiles][2 halves][128], row sum f32 [128]
 constexpr int kXchBytes = 2 * 2 * 128 * 2 + 128 * 4;
 // value CTA (rank 1)
-constexpr int kSub = 32;                   // cache rows per value-CTA stage
-constexpr int kBlk1 = kSub * 128;          // 4 KB
-constexpr int kStage1 = 8 * kBlk1;         // 32 KB
-constexpr int kStages1 = 4;
+constexpr int kSub = 64;                   // cache rows per value-CTA stage
+constexpr int kBlk1 = kSub * 128;          // 8 KB
+constexpr int kStage1 = 8 * kBlk1;         // 64 KB: one TMA box (fewer, larger boxes)
+constexpr int kStages1 = 2;
+constexpr int kStepsPerSub = kSub / 16;    // P . C K-steps per value-CTA stage
 constexpr int kOffP = kStages1 * kStage1;  // P slots [2], each P then alpha
 constexpr int kPSlot = 33 * 1024;          // slot stride (keeps P 1 KB aligned)
 // shared by both
@@ -333,13 +334,13 @@ __global__ void __launch_bounds__(kDecThreads, 1)
           fence_proxy_async_cta();  // tail rows were zeroed through the generic proxy
           const int nk = (ti.nvt + 15) >> 4;  // K-steps of 16 tokens
           const uint32_t pbase = smem_u32(smem + kOffP + slot * kPSlot);
-          for (int u = 0; u * 2 < nk; ++u, ++q) {
+          for (int u = 0; u * kStepsPerSub < nk; ++u, ++q) {
             const int st = q % kStages1;
             if (!mbar_wait(&bar[B_FULL + st], (uint32_t)(q / kStages1) & 1u, wc)) return false;
             tc_fence_after();
             const uint32_t sbase = smem_u32(smem + st * kStage1);
-            for (int kt = 0; kt < 2 && u * 2 + kt < nk; ++kt) {
-              const int gk = u * 2 + kt;
+            for (int kt = 0; kt < kStepsPerSub && u * kStepsPerSub + kt < nk; ++kt) {
+              const int gk = u * kStepsPerSub + kt;
               const uint64_t ad = smem_desc(pbase + (gk >> 2) * 16384 + (gk & 3) * 32, 16, 1024, 2);
 #pragma unroll
               for (int n = 0; n < 2; ++n) {  // N = 512 latent columns as 2 x 256
