@@ -47,6 +47,24 @@ def _peaks():
         return 6400.0, 1800.0, 1400.0, "fallback"
 
 
+def _decode_traffic():
+    """DRAM bytes per decode launch from the committed ncu summary, if the
+    decode kernel's sources are the ones that were profiled (else None)."""
+    import hashlib
+    import re
+    h = hashlib.sha256()
+    for f in ("decode.cuh", "sm100.cuh", "splitkv.cuh"):
+        with open(os.path.join(ROOT, "mla_latent_kv_68_b300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    key = h.hexdigest()[:16]
+    try:
+        with open(os.path.join(ROOT, "profiles", "decode_kernel_uniform_b32_s1_h128_l4096.md")) as f:
+            m = re.search(r"traffic-key: ([0-9a-f]+) bytes: (\d+)", f.read())
+    except OSError:
+        return None
+    return int(m.group(2)) if m and m.group(1) == key else None
+
+
 def _work(x):
     """Algorithmic bytes and flops of the decode kernel and of the whole step."""
     B, S, H = x["B"], x["S"], x["H"]
@@ -278,7 +296,8 @@ def run_ours(args, x, rank, world, local_rank):
         "config": _config(args, x),
         "roofline": {"kernel": "mla_decode (plan + decode kernels)", "bound": "hbm",
                      "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-                     "frac": round(achieved / hbm, 4), "traffic": None,
+                     "frac": round(achieved / hbm, 4),
+                     "traffic": _decode_traffic() if args.workload == DEFAULT_WORKLOAD else None,
                      "peak_source": src,
                      "tensor_tflops": round(wk["dec_flops"] / (dec_us * 1e-6) / 1e12, 1),
                      "tensor_frac_of_burst": round(wk["dec_flops"] / (dec_us * 1e-6) / 1e12 / tf_burst, 4)},
