@@ -18,13 +18,14 @@
 //       tensor memory as the A operand of the QK^T MMAs (A-from-TMEM form),
 //       next to one 128-column S buffer; shared memory is left to the TMA
 //       ring, whose depth sets how many bytes an SM keeps in flight.
-//       Every operand arrives through a 6-stage ring of 32 KB stages, each one TMA
-//       box of two 128-row x 64-column blocks (one 128-byte-swizzle atom per
-//       block): a tile is 5 stages (4 of c, 1 of k^R), and at a segment start
-//       the 128 query rows of q_cat pass through the same ring (5 stages) on
-//       their way into tensor memory.  The box size matters on B300: an SM's
-//       TMA unit sustains a few boxes per microsecond, so 16 KB boxes cap an
-//       SM near 50 GB/s while 32 KB boxes let half the SMs saturate HBM.
+//       Operands arrive through two TMA rings: a c ring of 64 KB stages, each
+//       one box of four 128-row x 64-column blocks (one 128-byte-swizzle atom
+//       per block), and a k^R ring of 16 KB stages; a tile is two c stages and
+//       one k^R stage, and at a segment start the 128 query rows of q_cat pass
+//       through the same rings on their way into tensor memory.  Box size and
+//       count matter on B300: an SM's TMA unit handles only a few boxes per
+//       microsecond, so 16 KB boxes cap an SM near 50 GB/s, 32 KB boxes near
+//       65-95 GB/s and 64 KB boxes near 100-120 GB/s.
 //       Eight softmax
 //       warps (two threads per query row, 64 tokens each) run the online
 //       softmax, write P (bf16, in the swizzled K-major layout the MMA reads)
@@ -65,10 +66,12 @@ constexpr int kDecThreads = 384;  // 12 warps: 0 TMA, 1 MMA, 2 P copy / release,
 constexpr int kTok = kTileRows;   // cache rows per tile (128)
 // score CTA (rank 0)
 constexpr int kBlk0 = kTok * 128;          // one block: 128 rows x 64 bf16 = 16 KB
-constexpr int kStage0 = 2 * kBlk0;         // one stage: two blocks (one TMA box)
-constexpr int kStages0 = 6;
-constexpr int kStagesPerTile = 5;          // c: 4 stages, k^R: 1 (q_cat: 4 + 1 for q^R)
-constexpr int kOffPS = kStages0 * kStage0; // P staging: 128 x 128 bf16 + rescale exponents[128]
+constexpr int kCStage = 4 * kBlk0;         // c ring stage: four blocks (one 64 KB TMA box)
+constexpr int kCStages = 2;
+constexpr int kRStage = kBlk0;             // k^R ring stage: one block (16 KB)
+constexpr int kRStages = 3;
+constexpr int kOffR = kCStages * kCStage;  // k^R ring
+constexpr int kOffPS = kOffR + kRStages * kRStage;  // P staging: 128 x 128 bf16 + rescale exponents[128]
 constexpr int kPBytes = 128 * kTok * 2;
 constexpr uint32_t kPTx = kPBytes + 128;      // bytes of one P slot with its exponent column
 constexpr int kOffXch = kOffPS + (int)kPTx;   // ceil(row max) int16 [2 tiles][2 halves][128], row sum f32 [128]
@@ -97,7 +100,7 @@ constexpr uint32_t kQRCol = 128;  // score CTA: q^R at columns 128..159; S at 0.
 
 // barrier indices
 enum : int {
-  B_FULL = 0, B_EMPTY = 10,          // TMA ring (rank 0: 5 stages, rank 1: 4)
+  B_FULL = 0, B_EMPTY = 10,          // TMA rings (rank 0: c at 0..1, k^R at 2..4; rank 1: 0..1)
   B_SFULL = 20, B_SEMPTY = 22,       // score CTA: S buffer (one; index 0 used)
   B_PEMPTY = 24,                     // score CTA: P slot in the value CTA free again
   B_QREADY = 26,                     // score CTA: Q of the segment is in place
@@ -156,12 +159,14 @@ __device__ __forceinline__ void for_each_tile(const DecodeParams& p, int g, F&& 
   }
 }
 
-// Score-CTA ring position of stage j of tile i in segment k: every segment
-// first sends its 5 query stages through the ring, every tile its 5 cache stages.
-__device__ __forceinline__ int ring_q_stage(int i, int k, int j) { return kStagesPerTile * (i + k) + j; }
-__device__ __forceinline__ int ring_kv_stage(int i, int k, int j) {
-  return kStagesPerTile * (i + k + 1) + j;
-}
+// Score-CTA ring positions for tile i of segment k.  Every segment first
+// sends its query rows through the rings (two c stages, one k^R stage),
+// every tile its cache rows (the same).  c stage h holds blocks 4h .. 4h + 3.
+__device__ __forceinline__ int cpos_q(int i, int k, int h) { return 2 * (i + k) + h; }
+__device__ __forceinline__ int cpos_kv(int i, int k, int h) { return 2 * (i + k + 1) + h; }
+__device__ __forceinline__ int rpos_q(int i, int k) { return i + k; }
+__device__ __forceinline__ int rpos_kv(int i, int k) { return i + k + 1; }
+constexpr int kBarC = 0, kBarR = kCStages;  // FULL / EMPTY sub-ranges of the two rings
 
 // All 32 lanes wait; the outcome is made warp-uniform so that warp-collective
 // tensor-memory instructions after it never run with a partial warp.
@@ -195,7 +200,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       *abort_flag = 1u;
       atomicOr(p.status, kDevErrInternal);
     }
-    for (int s = 0; s < kStages0; ++s) {
+    for (int s = 0; s < kCStages + kRStages; ++s) {
       mbar_init(&bar[B_FULL + s], 1);
       mbar_init(&bar[B_EMPTY + s], 1);
     }
@@ -244,47 +249,55 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   if (run && warp == 0) {
     // ------------------------------------------------ TMA producer (both CTAs)
     if (lane == 0) {
-      int last_use[kStages0];
-      for (int s = 0; s < kStages0; ++s) last_use[s] = -1;
-      const int nst = rank == 0 ? kStages0 : kStages1;
-      int q = 0;  // running stage counter
+      int last_use[kCStages + kRStages];
+      for (int s = 0; s < kCStages + kRStages; ++s) last_use[s] = -1;
+      int cq = 0, rq = 0, q = 0;  // running positions: score c ring, score k^R ring, value ring
+      // Issue one stage of a ring: wait for the slot, arm its barrier, copy.
+      auto slot = [&](int base, int nst, int pos, uint32_t bytes) -> int {
+        const int st = pos % nst;
+        if (!mbar_wait(&bar[B_EMPTY + base + st], ((uint32_t)(pos / nst) & 1u) ^ 1u, wc)) return -1;
+        mbar_arrive_expect_tx(&bar[B_FULL + base + st], bytes);
+        last_use[base + st] = pos;
+        return st;
+      };
       for_each_tile(p, g, [&](const TileInfo& ti) {
         const int row0 = ti.b * p.Lmax + ti.t * kTok;
         if (rank == 0) {
-          const int nstg = ti.first ? 2 * kStagesPerTile : kStagesPerTile;
-          const int qrow0 = ti.b * SH + rb * 128;
-          for (int j = 0; j < nstg; ++j, ++q) {
-            const int st = q % nst;
-            if (!mbar_wait(&bar[B_EMPTY + st], ((uint32_t)(q / nst) & 1u) ^ 1u, wc)) return false;
-            uint8_t* dst = smem + st * kStage0;
-            const int jj = ti.first ? j - kStagesPerTile : j;  // < 0: a query stage
-            const bool single = (jj == 4) || (jj == -1);      // k^R or q^R: one block
-            mbar_arrive_expect_tx(&bar[B_FULL + st], single ? kBlk0 : kStage0);
-            if (jj < -1)
-              tma_load_3d(dst, &tm_q, &bar[B_FULL + st], 0, qrow0, 2 * j);
-            else if (jj == -1)
-              tma_load_2d(dst, &tm_qr, &bar[B_FULL + st], 512, qrow0);
-            else if (jj < 4)
-              tma_load_3d(dst, &tm_c0, &bar[B_FULL + st], 0, row0, 2 * jj);
-            else
-              tma_load_2d(dst, &tm_kr, &bar[B_FULL + st], 0, row0);
-            last_use[st] = q;
+          if (ti.first) {  // the segment's query rows: blocks 0..7 through the c ring, q^R through k^R's
+            const int qrow0 = ti.b * SH + rb * 128;
+            for (int h = 0; h < 2; ++h, ++cq) {
+              const int st = slot(kBarC, kCStages, cq, kCStage);
+              if (st < 0) return false;
+              tma_load_3d(smem + st * kCStage, &tm_q, &bar[B_FULL + kBarC + st], 0, qrow0, 4 * h);
+            }
+            const int st = slot(kBarR, kRStages, rq++, kRStage);
+            if (st < 0) return false;
+            tma_load_2d(smem + kOffR + st * kRStage, &tm_qr, &bar[B_FULL + kBarR + st], 512, qrow0);
           }
+          for (int h = 0; h < 2; ++h, ++cq) {
+            const int st = slot(kBarC, kCStages, cq, kCStage);
+            if (st < 0) return false;
+            tma_load_3d(smem + st * kCStage, &tm_c0, &bar[B_FULL + kBarC + st], 0, row0, 4 * h);
+          }
+          const int st = slot(kBarR, kRStages, rq++, kRStage);
+          if (st < 0) return false;
+          tma_load_2d(smem + kOffR + st * kRStage, &tm_kr, &bar[B_FULL + kBarR + st], 0, row0);
         } else {
           const int nsub = (ti.nvt + kSub - 1) / kSub;
-          for (int u = 0; u < nsub; ++u, ++q) {  // 32-row stages of the 512 c columns
-            const int st = q % nst;
-            if (!mbar_wait(&bar[B_EMPTY + st], ((uint32_t)(q / nst) & 1u) ^ 1u, wc)) return false;
-            uint8_t* dst = smem + st * kStage1;
-            mbar_arrive_expect_tx(&bar[B_FULL + st], kStage1);
-            tma_load_3d(dst, &tm_c1, &bar[B_FULL + st], 0, row0 + u * kSub, 0);
-            last_use[st] = q;
+          for (int u = 0; u < nsub; ++u, ++q) {  // 64-row stages of the 512 c columns
+            const int st = slot(0, kStages1, q, kStage1);
+            if (st < 0) return false;
+            tma_load_3d(smem + st * kStage1, &tm_c1, &bar[B_FULL + st], 0, row0 + u * kSub, 0);
           }
         }
         return true;
       });
-      for (int s = 0; s < nst; ++s)  // let every issued copy land before the CTA winds down
-        if (last_use[s] >= 0) mbar_wait_drain(&bar[B_FULL + s], (uint32_t)(last_use[s] / nst) & 1u, wc);
+      // let every issued copy land before the CTA winds down
+      for (int s = 0; s < kCStages + kRStages; ++s) {
+        if (last_use[s] < 0) continue;
+        const int nst = rank == 0 ? (s < kBarR ? kCStages : kRStages) : kStages1;
+        mbar_wait_drain(&bar[B_FULL + s], (uint32_t)(last_use[s] / nst) & 1u, wc);
+      }
     }
   } else if (run && warp == 1) {
     // ------------------------------------------------ MMA issuer (one thread)
@@ -293,31 +306,35 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         constexpr uint32_t idesc = idesc_bf16_f32(128, kTok, 0, 0);
         for_each_tile(p, g, [&](const TileInfo& ti) {
           const uint32_t sph = (uint32_t)ti.i & 1u;  // the single S buffer, one phase per tile
-          if (ti.first) {  // the query stages have been moved out of the ring: release them
+          if (ti.first) {  // the query stages have been moved out of the rings: release them
             if (!mbar_wait(&bar[B_QREADY], (uint32_t)ti.k & 1u, wc)) return false;
-            for (int j = 0; j < kStagesPerTile; ++j)
-              mbar_arrive(&bar[B_EMPTY + ring_q_stage(ti.i, ti.k, j) % kStages0]);
+            for (int h = 0; h < 2; ++h) mbar_arrive(&bar[B_EMPTY + kBarC + cpos_q(ti.i, ti.k, h) % kCStages]);
+            mbar_arrive(&bar[B_EMPTY + kBarR + rpos_q(ti.i, ti.k) % kRStages]);
           }
           if (!mbar_wait(&bar[B_SEMPTY], sph ^ 1u, wc)) return false;
           const uint32_t d = tmem;
-          for (int j = 0; j < kStagesPerTile; ++j) {
-            const int q = ring_kv_stage(ti.i, ti.k, j), st = q % kStages0;
-            if (!mbar_wait(&bar[B_FULL + st], (uint32_t)(q / kStages0) & 1u, wc)) return false;
+          for (int h = 0; h < 2; ++h) {  // c blocks 4h .. 4h + 3 against q~ from tensor memory
+            const int q = cpos_kv(ti.i, ti.k, h), st = q % kCStages;
+            if (!mbar_wait(&bar[B_FULL + kBarC + st], (uint32_t)(q / kCStages) & 1u, wc)) return false;
             tc_fence_after();
-            const uint32_t sbase = smem_u32(smem + st * kStage0);
-            if (j < 4) {
+            const uint32_t sbase = smem_u32(smem + st * kCStage);
 #pragma unroll
-              for (int kk = 0; kk < 8; ++kk) {  // 2 blocks x 4 K-steps of 16
-                const int gk = j * 8 + kk;
-                const uint64_t bd = smem_desc(sbase + (kk >> 2) * kBlk0 + (kk & 3) * 32, 16, 1024, 2);
-                mma_ts(d, tmem + kQCol + (uint32_t)gk * 8, bd, idesc, gk > 0 ? 1u : 0u);
-              }
-            } else {
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk)  // k^R against q^R, both 64 wide
-                mma_ts(d, tmem + kQRCol + (uint32_t)kk * 8, smem_desc(sbase + kk * 32, 16, 1024, 2), idesc, 1u);
+            for (int kk = 0; kk < 16; ++kk) {  // 4 blocks x 4 K-steps of 16
+              const int gk = h * 16 + kk;
+              const uint64_t bd = smem_desc(sbase + (kk >> 2) * kBlk0 + (kk & 3) * 32, 16, 1024, 2);
+              mma_ts(d, tmem + kQCol + (uint32_t)gk * 8, bd, idesc, gk > 0 ? 1u : 0u);
             }
-            mma_commit(&bar[B_EMPTY + st]);
+            mma_commit(&bar[B_EMPTY + kBarC + st]);
+          }
+          {  // k^R against q^R, both 64 wide
+            const int q = rpos_kv(ti.i, ti.k), st = q % kRStages;
+            if (!mbar_wait(&bar[B_FULL + kBarR + st], (uint32_t)(q / kRStages) & 1u, wc)) return false;
+            tc_fence_after();
+            const uint32_t sbase = smem_u32(smem + kOffR + st * kRStage);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_ts(d, tmem + kQRCol + (uint32_t)kk * 8, smem_desc(sbase + kk * 32, 16, 1024, 2), idesc, 1u);
+            mma_commit(&bar[B_EMPTY + kBarR + st]);
           }
           mma_commit(&bar[B_SFULL]);
           return true;
@@ -408,9 +425,16 @@ __global__ void __launch_bounds__(kDecThreads, 1)
           // into its own buffer; the blocks come through the ring.
           limit = valid ? ti.L - p.S + s_r + 1 : 0;
           for (int j = hf * 4; j < hf * 4 + 4 + hf; ++j) {  // block j of the query row
-            const int q = ring_q_stage(ti.i, ti.k, j >> 1), st = q % kStages0;
-            if (!warp_wait(&bar[B_FULL + st], (uint32_t)(q / kStages0) & 1u, wc)) return false;
-            const uint8_t* rowp = smem + st * kStage0 + (j & 1) * kBlk0 + r * 128;
+            const uint8_t* rowp;
+            if (j < 8) {  // c stage hf, block j - 4 hf
+              const int q = cpos_q(ti.i, ti.k, hf), st = q % kCStages;
+              if (!warp_wait(&bar[B_FULL + kBarC + st], (uint32_t)(q / kCStages) & 1u, wc)) return false;
+              rowp = smem + st * kCStage + (j - 4 * hf) * kBlk0 + r * 128;
+            } else {      // q^R through the k^R ring
+              const int q = rpos_q(ti.i, ti.k), st = q % kRStages;
+              if (!warp_wait(&bar[B_FULL + kBarR + st], (uint32_t)(q / kRStages) & 1u, wc)) return false;
+              rowp = smem + kOffR + st * kRStage + r * 128;
+            }
             if (j < 8) {
               uint32_t v[32];
 #pragma unroll

@@ -112,7 +112,7 @@ bool encode_decode_maps(DecodeMaps* m, const void* q_cat, const void* c_kv, cons
                         int B, int S, int H, int Lmax) {
   const cuuint64_t rows = (cuuint64_t)B * Lmax, qrows = (cuuint64_t)B * S * H;
   const cuuint64_t c3d[3] = {64, rows, 8}, c3s[2] = {1024, 128};
-  const cuuint32_t c0b[3] = {64, (cuuint32_t)mla::kTok, 2}, c1b[3] = {64, (cuuint32_t)mla::kSub, 8};
+  const cuuint32_t c0b[3] = {64, (cuuint32_t)mla::kTok, 4}, c1b[3] = {64, (cuuint32_t)mla::kSub, 8};
   const cuuint64_t kd[2] = {64, rows}, ks[1] = {128};
   const cuuint32_t b2[2] = {64, (cuuint32_t)mla::kTok};
   const cuuint64_t q3d[3] = {64, qrows, 9}, q3s[2] = {1152, 128};
