@@ -10,6 +10,8 @@ from .oracle import (  # noqa: F401
     load,
     num_threads,
     rope,
+    rope_theta,
+    yarn_theta,
     decode,
     absorb,
     up_project,

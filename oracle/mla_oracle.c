@@ -27,6 +27,14 @@
  *   - positions are 0-based: keys sit at 0..L_b-1, query s of S sits at
  *     L_b - S + s and sees keys 0..L_b - S + s inclusive.
  *   - the cache holds the PRE-RoPE k_R; the oracle rotates it itself.
+ *   - YaRN ("YaRN 扩展", and "Long Context Extension" of the technical report
+ *     reading): theta'_j = (1 - g_j) theta_j / s + g_j theta_j, where g_j = 1
+ *     in the high-frequency band and 0 in the low one.  The pages give the band
+ *     edges only as alpha = 1, beta = 32; the ramp taken here is linear in the
+ *     number of turns a pair makes over the original context,
+ *     r_j = L_orig theta_j / (2 pi):  g_j = clamp((r_j - alpha) / (beta - alpha), 0, 1).
+ *     It applies to the whole decoupled RoPE branch (q^R and k^R), the only
+ *     place RoPE is used.
  *
  * The step functions below (absorb, latent attention, up-projection) restate
  * the absorbed identities of section "潜在向量的作用" (role of the latent
@@ -65,11 +73,36 @@ int mla_oracle_num_threads(void) {
 #endif
 }
 
-/* RoPE of one d_r-vector at integer position pos ("YaRN 扩展": phi_{m,j} = m theta_j). */
-static void rope_vec(const double *x, int d_r, double pos, double base, double *y) {
+/* theta_j = base^(-2j/d_r), j = 0 .. d_r/2 - 1 */
+static void base_theta(double base, int d_r, double *theta) {
+  for (int j = 0; j < d_r / 2; ++j) theta[j] = pow(base, -2.0 * (double)j / (double)d_r);
+}
+
+/*
+ * YaRN frequencies ("YaRN 扩展"): theta'_j = (1 - g_j) theta_j / s + g_j theta_j,
+ * g_j = 1 for pairs that turn many times over the original context (high
+ * frequency, kept), 0 for pairs that turn less than once (low frequency,
+ * divided by s), linear in between (see the reading above).
+ */
+int mla_oracle_yarn_theta(double base, int d_r, double s, double alpha, double beta,
+                          double orig_len, double *theta) {
+  if (d_r <= 0 || (d_r & 1) || !(s >= 1.0) || !(beta > alpha) || !(orig_len > 0.0)) return 1;
+  const double two_pi = 6.283185307179586476925286766559;
+  base_theta(base, d_r, theta);
   for (int j = 0; j < d_r / 2; ++j) {
-    double theta = pow(base, -2.0 * (double)j / (double)d_r);
-    double phi = pos * theta;
+    double r = orig_len * theta[j] / two_pi; /* turns over the original context */
+    double g = (r - alpha) / (beta - alpha);
+    if (g < 0.0) g = 0.0;
+    if (g > 1.0) g = 1.0;
+    theta[j] = (1.0 - g) * theta[j] / s + g * theta[j];
+  }
+  return 0;
+}
+
+/* RoPE of one d_r-vector at integer position pos ("YaRN 扩展": phi_{m,j} = m theta_j). */
+static void rope_vec(const double *x, int d_r, double pos, const double *theta, double *y) {
+  for (int j = 0; j < d_r / 2; ++j) {
+    double phi = pos * theta[j];
     double c = cos(phi), s = sin(phi);
     double x0 = x[2 * j], x1 = x[2 * j + 1];
     y[2 * j] = x0 * c - x1 * s;
@@ -77,18 +110,27 @@ static void rope_vec(const double *x, int d_r, double pos, double base, double *
   }
 }
 
-/* Public RoPE: x[n, d_r] rotated at positions pos[n]. */
-int mla_oracle_rope(const void *x, int dtype, const int64_t *pos, int n, int d_r,
-                    double base, double *out) {
+/* Public RoPE: x[n, d_r] rotated at positions pos[n] with frequencies theta[d_r/2]. */
+int mla_oracle_rope_theta(const void *x, int dtype, const int64_t *pos, int n, int d_r,
+                          const double *theta, double *out) {
   if (d_r <= 0 || (d_r & 1)) return 1;
   double *tmp = (double *)malloc(sizeof(double) * (size_t)d_r);
   if (!tmp) return 2;
   for (int r = 0; r < n; ++r) {
     for (int k = 0; k < d_r; ++k) tmp[k] = ld(x, (size_t)r * d_r + k, dtype);
-    rope_vec(tmp, d_r, (double)pos[r], base, out + (size_t)r * d_r);
+    rope_vec(tmp, d_r, (double)pos[r], theta, out + (size_t)r * d_r);
   }
   free(tmp);
   return 0;
+}
+
+/* The same with theta_j = base^(-2j/d_r). */
+int mla_oracle_rope(const void *x, int dtype, const int64_t *pos, int n, int d_r,
+                    double base, double *out) {
+  if (d_r <= 0 || (d_r & 1) || d_r > 1024) return 1;
+  double theta[512];
+  base_theta(base, d_r, theta);
+  return mla_oracle_rope_theta(x, dtype, pos, n, d_r, theta, out);
 }
 
 /*
@@ -97,16 +139,17 @@ int mla_oracle_rope(const void *x, int dtype, const int64_t *pos, int n, int d_r
  *   c_kv   [B,Lmax,d_c]  k_r    [B,Lmax,d_r] (pre-RoPE)
  *   W_UK   [H,d_h,d_c]   W_UV   [H,d_v,d_c]
  *   seqlens[B]
+ *   theta  : RoPE frequencies [d_r/2] (both q^R and k^R use them)
  *   rows   : flat indices (b*S + s)*H + h to compute (NULL -> all B*S*H rows)
  *   out    : [n_rows, d_v] fp64
  *   wsum   : optional [n_rows], the sum of the softmax weights of each row
  * Returns 0, or a nonzero code for an invalid argument.
  */
-int mla_oracle_decode(const void *q_nope, const void *q_rope, const void *c_kv,
-                      const void *k_r, const void *W_UK, const void *W_UV, int dtype,
-                      const int32_t *seqlens, int B, int S, int H, int Lmax, int d_c,
-                      int d_h, int d_r, int d_v, double softmax_scale, double rope_base,
-                      const int64_t *rows, int64_t n_rows, double *out, double *wsum) {
+int mla_oracle_decode_theta(const void *q_nope, const void *q_rope, const void *c_kv,
+                            const void *k_r, const void *W_UK, const void *W_UV, int dtype,
+                            const int32_t *seqlens, int B, int S, int H, int Lmax, int d_c,
+                            int d_h, int d_r, int d_v, double softmax_scale, const double *theta,
+                            const int64_t *rows, int64_t n_rows, double *out, double *wsum) {
   if (B <= 0 || S <= 0 || H <= 0 || Lmax <= 0 || d_c <= 0 || d_h <= 0 || d_r < 0 ||
       (d_r & 1) || d_v <= 0)
     return 1;
@@ -144,7 +187,7 @@ int mla_oracle_decode(const void *q_nope, const void *q_rope, const void *c_kv,
       size_t qoff = (((size_t)b * S + s) * H + h);
       for (int d = 0; d < d_h; ++d) qn[d] = ld(q_nope, qoff * d_h + d, dtype);
       for (int d = 0; d < d_r; ++d) qr_raw[d] = ld(q_rope, qoff * d_r + d, dtype);
-      rope_vec(qr_raw, d_r, (double)pos_q, rope_base, qr);
+      rope_vec(qr_raw, d_r, (double)pos_q, theta, qr);
 
       /* pass 1: every score, with the key expanded per head */
       for (int j = 0; j < nvis; ++j) {
@@ -157,7 +200,7 @@ int mla_oracle_decode(const void *q_nope, const void *q_rope, const void *c_kv,
           kc[d] = acc;
         }
         for (int d = 0; d < d_r; ++d) kr_raw[d] = ld(k_r, coff * d_r + d, dtype);
-        rope_vec(kr_raw, d_r, (double)j, rope_base, kr); /* k^R_j = RoPE_j(.) */
+        rope_vec(kr_raw, d_r, (double)j, theta, kr); /* k^R_j = RoPE_j(.) */
         double dot = 0.0;
         for (int d = 0; d < d_h; ++d) dot += qn[d] * kc[d];
         for (int d = 0; d < d_r; ++d) dot += qr[d] * kr[d];
@@ -191,6 +234,20 @@ int mla_oracle_decode(const void *q_nope, const void *q_rope, const void *c_kv,
     free(c); free(kc); free(vc); free(score);
   }
   return bad;
+}
+
+/* The same with theta_j = rope_base^(-2j/d_r). */
+int mla_oracle_decode(const void *q_nope, const void *q_rope, const void *c_kv,
+                      const void *k_r, const void *W_UK, const void *W_UV, int dtype,
+                      const int32_t *seqlens, int B, int S, int H, int Lmax, int d_c,
+                      int d_h, int d_r, int d_v, double softmax_scale, double rope_base,
+                      const int64_t *rows, int64_t n_rows, double *out, double *wsum) {
+  if (d_r < 0 || d_r > 1024) return 1;
+  double theta[512];
+  base_theta(rope_base, d_r, theta);
+  return mla_oracle_decode_theta(q_nope, q_rope, c_kv, k_r, W_UK, W_UV, dtype, seqlens, B, S, H,
+                                 Lmax, d_c, d_h, d_r, d_v, softmax_scale, theta, rows, n_rows,
+                                 out, wsum);
 }
 
 /*

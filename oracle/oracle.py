@@ -41,6 +41,10 @@ def load():
         vp, i32, i64, f64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_double
         lib.mla_oracle_num_threads.restype = i32
         lib.mla_oracle_rope.argtypes = [vp, i32, vp, i32, i32, f64, vp]
+        lib.mla_oracle_rope_theta.argtypes = [vp, i32, vp, i32, i32, vp, vp]
+        lib.mla_oracle_yarn_theta.argtypes = [f64, i32, f64, f64, f64, f64, vp]
+        lib.mla_oracle_decode_theta.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32,
+                                                i32, i32, i32, i32, i32, f64, vp, vp, i64, vp, vp]
         lib.mla_oracle_decode.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32,
                                           i32, i32, i32, i32, f64, f64, vp, i64, vp, vp]
         lib.mla_oracle_absorb.argtypes = [vp, vp, i32, i32, i32, i32, i32, vp]
@@ -48,7 +52,8 @@ def load():
         lib.mla_oracle_latent_attention.argtypes = [vp, vp, vp, i32, vp, i32, i32, i32, i32,
                                                     i32, i32, f64, vp, i64, vp]
         for name in ("mla_oracle_rope", "mla_oracle_decode", "mla_oracle_absorb",
-                     "mla_oracle_up_project", "mla_oracle_latent_attention"):
+                     "mla_oracle_up_project", "mla_oracle_latent_attention",
+                     "mla_oracle_rope_theta", "mla_oracle_yarn_theta", "mla_oracle_decode_theta"):
             getattr(lib, name).restype = i32
         _lib = lib
     return _lib
@@ -92,8 +97,30 @@ def rope(x, pos, base: float = 10000.0):
     return out
 
 
+def yarn_theta(d_r: int = 64, *, base: float = 10000.0, s: float = 40.0, alpha: float = 1.0,
+               beta: float = 32.0, orig_len: float = 4096.0):
+    """YaRN RoPE frequencies theta'_j (section "YaRN 扩展"), fp64 [d_r/2]."""
+    out = np.empty(d_r // 2, np.float64)
+    _check(load().mla_oracle_yarn_theta(float(base), d_r, float(s), float(alpha), float(beta),
+                                        float(orig_len), _ptr(out)), "yarn_theta")
+    return out
+
+
+def rope_theta(x, pos, theta):
+    """RoPE of x[n, d_r] at positions pos[n] with explicit frequencies theta[d_r/2]."""
+    a, code = _arr(x)
+    n, d_r = a.shape
+    p = np.ascontiguousarray(pos, dtype=np.int64)
+    th = np.ascontiguousarray(theta, dtype=np.float64)
+    assert p.shape == (n,) and th.shape == (d_r // 2,)
+    out = np.empty((n, d_r), np.float64)
+    _check(load().mla_oracle_rope_theta(_ptr(a), code, _ptr(p), n, d_r, _ptr(th), _ptr(out)),
+           "rope_theta")
+    return out
+
+
 def decode(q_nope, q_rope, c_kv, k_r, W_UK, W_UV, seqlens, *, softmax_scale=None,
-           rope_base: float = 10000.0, rows=None, return_wsum: bool = False):
+           rope_base: float = 10000.0, rope_theta=None, rows=None, return_wsum: bool = False):
     """Unabsorbed MLA decode.  Shapes: q_nope [B,S,H,d_h], q_rope [B,S,H,d_r],
     c_kv [B,Lmax,d_c], k_r [B,Lmax,d_r] (pre-RoPE), W_UK [H,d_h,d_c],
     W_UV [H,d_v,d_c], seqlens [B].  Returns out [n_rows, d_v] for the flat rows
@@ -121,10 +148,18 @@ def decode(q_nope, q_rope, c_kv, k_r, W_UK, W_UV, seqlens, *, softmax_scale=None
         n_rows, rp = rows.shape[0], _ptr(rows)
     out = np.empty((n_rows, d_v), np.float64)
     wsum = np.empty((n_rows,), np.float64)
-    rc = load().mla_oracle_decode(_ptr(qn), _ptr(qr), _ptr(ck), _ptr(kr), _ptr(wk), _ptr(wv),
-                                  code, _ptr(sl), B, S, H, Lmax, d_c, d_h, d_r, d_v,
-                                  float(softmax_scale), float(rope_base), rp, n_rows,
-                                  _ptr(out), _ptr(wsum))
+    if rope_theta is None:
+        rc = load().mla_oracle_decode(_ptr(qn), _ptr(qr), _ptr(ck), _ptr(kr), _ptr(wk), _ptr(wv),
+                                      code, _ptr(sl), B, S, H, Lmax, d_c, d_h, d_r, d_v,
+                                      float(softmax_scale), float(rope_base), rp, n_rows,
+                                      _ptr(out), _ptr(wsum))
+    else:
+        th = np.ascontiguousarray(rope_theta, dtype=np.float64)
+        assert th.shape == (d_r // 2,)
+        rc = load().mla_oracle_decode_theta(_ptr(qn), _ptr(qr), _ptr(ck), _ptr(kr), _ptr(wk),
+                                            _ptr(wv), code, _ptr(sl), B, S, H, Lmax, d_c, d_h,
+                                            d_r, d_v, float(softmax_scale), _ptr(th), rp, n_rows,
+                                            _ptr(out), _ptr(wsum))
     _check(rc, "decode")
     if rows is None:
         out = out.reshape(B, S, H, d_v)
