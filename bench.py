@@ -134,10 +134,14 @@ class ClockSampler:
                 "samples": len(rows)}
 
 
-def _oracle_sample(x, seconds: float, seed: int = 0):
+def _oracle_sample(x, seconds: float, seed: int = 0, rope: str = "plain"):
     """Time the oracle on a bounded random sample of output rows; return the
     extrapolated whole-step time in us, the thread count and the sample text."""
     import oracle
+    kw = {}
+    if rope == "yarn":
+        kw = dict(rope_theta=oracle.yarn_theta(64),
+                  softmax_scale=(0.1 * math.log(40.0) + 1.0) / math.sqrt(192.0))
     threads = oracle.num_threads()
     b = {k: bf16_bits(x[k]) for k in ("q_nope", "q_rope", "c_kv", "k_r", "W_UK", "W_UV")}
     total = x["B"] * x["S"] * x["H"]
@@ -149,14 +153,14 @@ def _oracle_sample(x, seconds: float, seed: int = 0):
     rows = rng.choice(total, n, replace=False)
     t0 = time.perf_counter()
     oracle.decode(b["q_nope"], b["q_rope"], b["c_kv"], b["k_r"], b["W_UK"], b["W_UV"],
-                  x["seqlens"].numpy(), rows=rows)
+                  x["seqlens"].numpy(), rows=rows, **kw)
     dt = time.perf_counter() - t0
     if dt < seconds and n < total:
         n2 = int(min(total, max(n, n * seconds / max(dt, 1e-3))))
         rows = rng.choice(total, n2, replace=False)
         t0 = time.perf_counter()
         oracle.decode(b["q_nope"], b["q_rope"], b["c_kv"], b["k_r"], b["W_UK"], b["W_UV"],
-                      x["seqlens"].numpy(), rows=rows)
+                      x["seqlens"].numpy(), rows=rows, **kw)
         dt = time.perf_counter() - t0
         n = n2
     # extrapolate by visible tokens (the oracle's cost is linear in them)
@@ -171,7 +175,7 @@ def run_reference(args, x, rank, world):
         return
     per_step = []
     for i in range(args.warmup + args.steps):
-        us, threads, sample = _oracle_sample(x, seconds=args.ref_seconds, seed=i)
+        us, threads, sample = _oracle_sample(x, seconds=args.ref_seconds, seed=i, rope=args.rope)
         if i >= args.warmup:
             per_step.append(us)
     v = statistics.mean(per_step)
@@ -195,7 +199,9 @@ def _config(args, x):
             "L": w.L if w.L is not None else f"U[{w.L_range[0]},{w.L_range[1]}]",
             "sum_L": int(x["seqlens"].sum()), "d_c": 512, "d_rope": 64,
             "l2": "flushed between timed steps (256 MiB write, then 256 MiB read)",
-            "parallelism": f"replicas x{args.gpus}" if args.gpus > 1 else "single GPU"}
+            "parallelism": f"replicas x{args.gpus}" if args.gpus > 1 else "single GPU",
+            "rope": ("yarn (s=40, alpha=1, beta=32, original 4096; score scale 0.1 ln s + 1)"
+                     if getattr(args, "rope", "plain") == "yarn" else "plain (base 10000)")}
 
 
 def run_ours(args, x, rank, world, local_rank):
@@ -205,8 +211,10 @@ def run_ours(args, x, rank, world, local_rank):
     torch.cuda.set_device(dev)
     mb.lib()
     d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
-    mb.rope_cache(d["k_r"], d["seqlens"])          # cache fill: keys rotated once (untimed)
-    step = mb.DecodeStep(x["B"], x["S"], x["H"], device=dev)
+    theta = mb.yarn_frequencies() if args.rope == "yarn" else None
+    scale = mb.yarn_softmax_scale() if args.rope == "yarn" else mb.SOFTMAX_SCALE
+    mb.rope_cache(d["k_r"], d["seqlens"], theta=theta)  # cache fill: keys rotated once (untimed)
+    step = mb.DecodeStep(x["B"], x["S"], x["H"], device=dev, rope_theta=theta, softmax_scale=scale)
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     flush_read = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
@@ -314,7 +322,7 @@ def run_ours(args, x, rank, world, local_rank):
         "clocks": clocks.summary(),
     }
     if not args.quick and world == 1:
-        us, threads, sample = _oracle_sample(x, seconds=args.ref_seconds)
+        us, threads, sample = _oracle_sample(x, seconds=args.ref_seconds, rope=args.rope)
         line["cpu_baseline"] = {"value": round(us, 1), "unit": "us/step", "cores": threads,
                                 "kind": "oracle", "sample": sample}
     print(json.dumps(line), flush=True)
@@ -343,6 +351,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--quick", action="store_true", help="skip the CPU-baseline timing")
     ap.add_argument("--ref-seconds", type=float, default=12.0)
+    ap.add_argument("--rope", default="plain", choices=["plain", "yarn"],
+                    help="RoPE frequencies of the step (yarn: the long-context setting)")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be >= 3")

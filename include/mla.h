@@ -122,6 +122,36 @@ mla_status mla_rope_apply(const mla_bf16 *x_in, int64_t in_stride_n, int64_t in_
                           float base, void *stream);
 
 /*
+ * RoPE with caller-given frequencies instead of base^(-2i/64): the same as
+ * mla_rope_apply, with theta[32] a HOST array of the 32 pair frequencies
+ * (finite, > 0), read during the call.  Used for YaRN (below).
+ */
+mla_status mla_rope_apply_freq(const mla_bf16 *x_in, int64_t in_stride_n, int64_t in_stride_h,
+                               mla_bf16 *x_out, int64_t out_stride_n, int64_t out_stride_h,
+                               int64_t N, int nh, int pos_mode, const int32_t *pos_src, int group,
+                               const double *theta, void *stream);
+
+/* mla_absorb_rope_q with caller-given frequencies theta[32] (host array). */
+mla_status mla_absorb_rope_q_freq(const mla_bf16 *q_nope, const mla_bf16 *q_rope,
+                                  const mla_bf16 *W_UK, const int32_t *seqlens, mla_bf16 *q_cat,
+                                  int B, int S, int H, const double *theta, void *stream);
+
+/*
+ * YaRN frequencies ("YaRN 扩展": theta'_j = (1 - g_j) theta_j / s + g_j theta_j,
+ * g_j = 1 for the high-frequency pairs, 0 for the low-frequency ones; the
+ * technical report's long-context setting is s = 40, alpha = 1, beta = 32 over
+ * an original context of 4096).  g_j is taken linear in the number of turns
+ * r_j = orig_len * theta_j / (2 pi) a pair makes over the original context,
+ * clamped to [0, 1] between alpha and beta turns; theta_j = base^(-2j/64).
+ * Host-only arithmetic; writes theta[0..31].  Returns MLA_OK or
+ * MLA_ERR_INVALID_ARG.  Use the result for the queries' and the cache's RoPE
+ * alike, and scale the scores by (0.1 ln s + 1): softmax_scale =
+ * (0.1 ln s + 1) / sqrt(192) in mla_decode.
+ */
+int mla_rope_yarn_frequencies(double base, double s, double alpha, double beta, double orig_len,
+                              double *theta);
+
+/*
  * Bytes of device workspace mla_decode needs for this shape on the current
  * device (it depends on the device's SM count).  0 if the shape is
  * unsupported or no device is present.  The workspace carries the device

@@ -53,6 +53,10 @@ def lib():
         L.mla_version.restype = i32
         L.mla_absorb_q.argtypes = [vp, vp, vp, i32, i32, i32, vp]
         L.mla_absorb_rope_q.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, f32, vp]
+        L.mla_absorb_rope_q_freq.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, vp, vp]
+        L.mla_rope_apply_freq.argtypes = [vp, i64, i64, vp, i64, i64, i64, i32, i32, vp, i32, vp, vp]
+        f64 = ctypes.c_double
+        L.mla_rope_yarn_frequencies.argtypes = [f64, f64, f64, f64, f64, vp]
         L.mla_rope_apply.argtypes = [vp, i64, i64, vp, i64, i64, i64, i32, i32, vp, i32, f32, vp]
         L.mla_decode_workspace_size.restype = sz
         L.mla_decode_workspace_size.argtypes = [i32, i32, i32]
@@ -61,7 +65,8 @@ def lib():
         L.mla_up_project.argtypes = [vp, vp, vp, i32, i32, i32, vp]
         L.mla_read_status.argtypes = [vp, vp]
         L.mla_decode_noalloc.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, f32, vp, vp]
-        for n in ("mla_absorb_q", "mla_absorb_rope_q", "mla_rope_apply", "mla_decode",
+        for n in ("mla_absorb_q", "mla_absorb_rope_q", "mla_absorb_rope_q_freq", "mla_rope_apply",
+                  "mla_rope_apply_freq", "mla_rope_yarn_frequencies", "mla_decode",
                   "mla_splitkv_combine", "mla_up_project", "mla_read_status",
                   "mla_decode_noalloc"):
             getattr(L, n).restype = i32
@@ -112,32 +117,65 @@ def absorb_q(q_nope, W_UK, q_cat, stream=None):
            "mla_absorb_q")
 
 
-def absorb_rope_q(q_nope, q_rope, W_UK, seqlens, q_cat, base=ROPE_BASE, stream=None):
+def yarn_frequencies(s=40.0, alpha=1.0, beta=32.0, orig_len=4096.0, base=ROPE_BASE):
+    """YaRN RoPE frequencies (32 pairs, float64) from mla_rope_yarn_frequencies;
+    the defaults are the pages' long-context setting."""
+    out = (ctypes.c_double * 32)()
+    _check(lib().mla_rope_yarn_frequencies(base, s, alpha, beta, orig_len, out),
+           "mla_rope_yarn_frequencies")
+    return [float(v) for v in out]
+
+
+def yarn_softmax_scale(s=40.0):
+    """Score scale with YaRN's attention factor 0.1 ln s + 1 on 1/sqrt(192)."""
+    return (0.1 * math.log(s) + 1.0) * SOFTMAX_SCALE
+
+
+def _theta_arg(theta):
+    if len(theta) != 32:
+        raise ValueError("theta must hold 32 frequencies")
+    return (ctypes.c_double * 32)(*[float(v) for v in theta])
+
+
+def absorb_rope_q(q_nope, q_rope, W_UK, seqlens, q_cat, base=ROPE_BASE, theta=None, stream=None):
     """q_cat[..., :512] = W_UK[h]^T q_nope and q_cat[..., 512:] = RoPE(q_rope) at
-    positions seqlens[b] - S + s, in one launch."""
+    positions seqlens[b] - S + s, in one launch (frequencies from `base`, or
+    the 32 given in `theta`)."""
     B, S, H, _ = q_nope.shape
     _need(q_nope, "q_nope", shape=(B, S, H, D_H))
     _need(q_rope, "q_rope", shape=(B, S, H, D_R))
     _need(W_UK, "W_UK", shape=(H, D_H, D_C))
     _need(seqlens, "seqlens", dtype=torch.int32, shape=(B,))
     _need(q_cat, "q_cat", shape=(B, S, H, D_QK))
-    _check(lib().mla_absorb_rope_q(_ptr(q_nope), _ptr(q_rope), _ptr(W_UK), _ptr(seqlens),
-                                   _ptr(q_cat), B, S, H, base, _stream(stream)),
-           "mla_absorb_rope_q")
+    if theta is None:
+        _check(lib().mla_absorb_rope_q(_ptr(q_nope), _ptr(q_rope), _ptr(W_UK), _ptr(seqlens),
+                                       _ptr(q_cat), B, S, H, base, _stream(stream)),
+               "mla_absorb_rope_q")
+    else:
+        _check(lib().mla_absorb_rope_q_freq(_ptr(q_nope), _ptr(q_rope), _ptr(W_UK), _ptr(seqlens),
+                                            _ptr(q_cat), B, S, H, _theta_arg(theta),
+                                            _stream(stream)), "mla_absorb_rope_q_freq")
 
 
 def rope_apply(x_in, in_stride_n, in_stride_h, x_out, out_stride_n, out_stride_h, N, nh,
-               pos_mode, pos_src, group=1, base=ROPE_BASE, stream=None):
-    """Raw mla_rope_apply (strides in elements)."""
+               pos_mode, pos_src, group=1, base=ROPE_BASE, stream=None, theta=None):
+    """Raw mla_rope_apply (strides in elements); mla_rope_apply_freq when the
+    32 frequencies `theta` are given."""
     if x_in.dtype != torch.bfloat16 or x_out.dtype != torch.bfloat16:
         raise TypeError("rope tensors must be bf16")
     _need(pos_src, "pos_src", dtype=torch.int32)
-    _check(lib().mla_rope_apply(_ptr(x_in), in_stride_n, in_stride_h, _ptr(x_out), out_stride_n,
-                                out_stride_h, N, nh, pos_mode, _ptr(pos_src), group, base,
-                                _stream(stream)), "mla_rope_apply")
+    if theta is None:
+        _check(lib().mla_rope_apply(_ptr(x_in), in_stride_n, in_stride_h, _ptr(x_out),
+                                    out_stride_n, out_stride_h, N, nh, pos_mode, _ptr(pos_src),
+                                    group, base, _stream(stream)), "mla_rope_apply")
+    else:
+        _check(lib().mla_rope_apply_freq(_ptr(x_in), in_stride_n, in_stride_h, _ptr(x_out),
+                                         out_stride_n, out_stride_h, N, nh, pos_mode,
+                                         _ptr(pos_src), group, _theta_arg(theta),
+                                         _stream(stream)), "mla_rope_apply_freq")
 
 
-def rope_queries(q_rope, q_cat, seqlens, base=ROPE_BASE, stream=None):
+def rope_queries(q_rope, q_cat, seqlens, base=ROPE_BASE, stream=None, theta=None):
     """q_cat[..., 512:] = RoPE(q_rope) at positions seqlens[b] - S + s."""
     B, S, H, _ = q_rope.shape
     _need(q_rope, "q_rope", shape=(B, S, H, D_R))
@@ -145,15 +183,16 @@ def rope_queries(q_rope, q_cat, seqlens, base=ROPE_BASE, stream=None):
     _need(seqlens, "seqlens", dtype=torch.int32, shape=(B,))
     out = q_cat.view(-1)[D_C:]
     rope_apply(q_rope, H * D_R, D_R, out, H * D_QK, D_QK, B * S, H, POS_QUERY, seqlens, S, base,
-               stream)
+               stream, theta)
 
 
-def rope_cache(k_r, seqlens, base=ROPE_BASE, stream=None):
+def rope_cache(k_r, seqlens, base=ROPE_BASE, stream=None, theta=None):
     """Rotate the cached k_R [B,Lmax,64] in place at positions 0..seqlens[b]-1."""
     B, Lmax, _ = k_r.shape
     _need(k_r, "k_r", shape=(B, Lmax, D_R))
     _need(seqlens, "seqlens", dtype=torch.int32, shape=(B,))
-    rope_apply(k_r, D_R, 0, k_r, D_R, 0, B * Lmax, 1, POS_CACHE, seqlens, Lmax, base, stream)
+    rope_apply(k_r, D_R, 0, k_r, D_R, 0, B * Lmax, 1, POS_CACHE, seqlens, Lmax, base, stream,
+               theta)
 
 
 def decode_workspace_size(B: int, S: int, H: int) -> int:
@@ -226,15 +265,21 @@ class DecodeStep:
     four library calls of a step on one stream:
     absorb + RoPE(queries) -> decode -> combine -> up-project."""
 
-    def __init__(self, B: int, S: int, H: int, device="cuda"):
+    def __init__(self, B: int, S: int, H: int, device="cuda", rope_theta=None,
+                 softmax_scale=SOFTMAX_SCALE):
+        """rope_theta: 32 RoPE frequencies for the queries (e.g. yarn_frequencies());
+        None for base 10000.  The cache's k_R must be rotated with the same ones.
+        softmax_scale: the score scale used when a call passes none."""
         self.B, self.S, self.H = B, S, H
+        self.rope_theta = rope_theta
+        self.softmax_scale = softmax_scale
         self.q_cat = torch.empty(B, S, H, D_QK, dtype=torch.bfloat16, device=device)
         self.o_lat = torch.empty(B, S, H, D_C, dtype=torch.bfloat16, device=device)
         self.out = torch.empty(B, S, H, D_V, dtype=torch.bfloat16, device=device)
         self.workspace = new_workspace(B, S, H, device)
 
     def __call__(self, q_nope, q_rope, c_kv, k_r, seqlens, W_UK, W_UV,
-                 softmax_scale=SOFTMAX_SCALE, stream=None):
+                 softmax_scale=None, stream=None):
         self.queries(q_nope, q_rope, seqlens, W_UK, stream)
         self.attend(c_kv, k_r, seqlens, softmax_scale, stream)
         self.project(W_UV, stream)
@@ -242,10 +287,12 @@ class DecodeStep:
 
     # The three phases of a step, separately callable for per-phase timing.
     def queries(self, q_nope, q_rope, seqlens, W_UK, stream=None):
-        absorb_rope_q(q_nope, q_rope, W_UK, seqlens, self.q_cat, stream=stream)
+        absorb_rope_q(q_nope, q_rope, W_UK, seqlens, self.q_cat, theta=self.rope_theta,
+                      stream=stream)
 
-    def attend(self, c_kv, k_r, seqlens, softmax_scale=SOFTMAX_SCALE, stream=None):
-        decode(self.q_cat, c_kv, k_r, seqlens, self.workspace, softmax_scale, stream)
+    def attend(self, c_kv, k_r, seqlens, softmax_scale=None, stream=None):
+        scale = self.softmax_scale if softmax_scale is None else softmax_scale
+        decode(self.q_cat, c_kv, k_r, seqlens, self.workspace, scale, stream)
 
     def project(self, W_UV, stream=None):
         splitkv_combine(self.workspace, self.o_lat, stream)

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -218,8 +219,8 @@ namespace {
 
 // Shared body of mla_absorb_q and mla_absorb_rope_q (q_rope == nullptr: no RoPE).
 mla_status absorb_launch(const mla_bf16* q_nope, const mla_bf16* q_rope, const mla_bf16* W_UK,
-                         const int32_t* seqlens, mla_bf16* q_cat, int B, int S, int H, float base,
-                         void* stream) {
+                         const int32_t* seqlens, mla_bf16* q_cat, int B, int S, int H,
+                         const mla::RopeTheta& th, void* stream) {
   if (!q_nope || !W_UK || !q_cat || !aligned16(q_nope) || !aligned16(W_UK) || !aligned16(q_cat))
     return MLA_ERR_INVALID_ARG;
   if (B < 1 || S < 1 || H < 1) return MLA_ERR_INVALID_ARG;
@@ -250,37 +251,36 @@ mla_status absorb_launch(const mla_bf16* q_nope, const mla_bf16* q_rope, const m
   p.tmem_cols = pow2_at_least((uint32_t)(2 * n_tile));
   p.status = dev->kernel_status;
   p.timeout_ns = kTimeoutNs;
-  mla::RopeTheta th;
-  for (int j = 0; j < 32; ++j) th.theta[j] = std::pow((double)base, -2.0 * j / 64.0);
   const dim3 grid(H, 2, (unsigned)((BS + n_tile - 1) / n_tile));
   mla::absorb_kernel<<<grid, mla::kAbsorbThreads, mla::absorb_smem_bytes(n_tile),
                        (cudaStream_t)stream>>>(tw, tq, p, th);
   return launch_status();
 }
 
-}  // namespace
-
-extern "C" {
-
-mla_status mla_absorb_q(const mla_bf16* q_nope, const mla_bf16* W_UK, mla_bf16* q_cat, int B,
-                        int S, int H, void* stream) {
-  return absorb_launch(q_nope, nullptr, W_UK, nullptr, q_cat, B, S, H, 10000.0f, stream);
+// theta_j = base^(-2j/64)
+mla::RopeTheta base_theta(double base) {
+  mla::RopeTheta th;
+  for (int j = 0; j < 32; ++j) th.theta[j] = std::pow(base, -2.0 * j / 64.0);
+  return th;
 }
 
-mla_status mla_absorb_rope_q(const mla_bf16* q_nope, const mla_bf16* q_rope, const mla_bf16* W_UK,
-                             const int32_t* seqlens, mla_bf16* q_cat, int B, int S, int H,
-                             float base, void* stream) {
-  if (!q_rope || !seqlens || !aligned16(q_rope)) return MLA_ERR_INVALID_ARG;
-  if (!(base > 1.0f) || !std::isfinite(base)) return MLA_ERR_INVALID_ARG;
-  return absorb_launch(q_nope, q_rope, W_UK, seqlens, q_cat, B, S, H, base, stream);
+// Caller-given frequencies: finite and positive.
+bool copy_theta(const double* theta, mla::RopeTheta* th) {
+  if (!theta) return false;
+  for (int j = 0; j < 32; ++j) {
+    if (!(theta[j] > 0.0) || !std::isfinite(theta[j])) return false;
+    th->theta[j] = theta[j];
+  }
+  return true;
 }
 
-mla_status mla_rope_apply(const mla_bf16* x_in, int64_t in_stride_n, int64_t in_stride_h,
-                          mla_bf16* x_out, int64_t out_stride_n, int64_t out_stride_h, int64_t N,
-                          int nh, int pos_mode, const int32_t* pos_src, int group, float base,
-                          void* stream) {
+// mla_rope_apply with the frequencies already formed.
+mla_status rope_launch(const mla_bf16* x_in, int64_t in_stride_n, int64_t in_stride_h,
+                       mla_bf16* x_out, int64_t out_stride_n, int64_t out_stride_h, int64_t N,
+                       int nh, int pos_mode, const int32_t* pos_src, int group,
+                       const mla::RopeTheta& th, void* stream) {
   if (!x_in || !x_out || !pos_src || !aligned16(x_in) || !aligned16(x_out)) return MLA_ERR_INVALID_ARG;
-  if (N < 0 || nh < 1 || !(base > 1.0f) || !std::isfinite(base)) return MLA_ERR_INVALID_ARG;
+  if (N < 0 || nh < 1) return MLA_ERR_INVALID_ARG;
   if ((in_stride_n | in_stride_h | out_stride_n | out_stride_h) & 7) return MLA_ERR_INVALID_ARG;
   if (in_stride_n < 0 || in_stride_h < 0 || out_stride_n < 0 || out_stride_h < 0)
     return MLA_ERR_INVALID_ARG;
@@ -288,8 +288,6 @@ mla_status mla_rope_apply(const mla_bf16* x_in, int64_t in_stride_n, int64_t in_
     return MLA_ERR_INVALID_ARG;
   if (pos_mode != mla::kPosExplicit && group < 1) return MLA_ERR_INVALID_ARG;
   if (N == 0) return MLA_OK;
-  mla::RopeTheta th;
-  for (int j = 0; j < 32; ++j) th.theta[j] = std::pow((double)base, -2.0 * j / 64.0);
   const long long threads = N * (long long)nh * 8;
   const int block = 256;
   const long long grid = (threads + block - 1) / block;
@@ -299,6 +297,68 @@ mla_status mla_rope_apply(const mla_bf16* x_in, int64_t in_stride_n, int64_t in_
       reinterpret_cast<__nv_bfloat16*>(x_out), out_stride_n, out_stride_h, N, nh, pos_mode,
       pos_src, group, th);
   return launch_status();
+}
+
+}  // namespace
+
+extern "C" {
+
+mla_status mla_absorb_q(const mla_bf16* q_nope, const mla_bf16* W_UK, mla_bf16* q_cat, int B,
+                        int S, int H, void* stream) {
+  return absorb_launch(q_nope, nullptr, W_UK, nullptr, q_cat, B, S, H, base_theta(10000.0), stream);
+}
+
+mla_status mla_absorb_rope_q(const mla_bf16* q_nope, const mla_bf16* q_rope, const mla_bf16* W_UK,
+                             const int32_t* seqlens, mla_bf16* q_cat, int B, int S, int H,
+                             float base, void* stream) {
+  if (!q_rope || !seqlens || !aligned16(q_rope)) return MLA_ERR_INVALID_ARG;
+  if (!(base > 1.0f) || !std::isfinite(base)) return MLA_ERR_INVALID_ARG;
+  return absorb_launch(q_nope, q_rope, W_UK, seqlens, q_cat, B, S, H, base_theta(base), stream);
+}
+
+mla_status mla_absorb_rope_q_freq(const mla_bf16* q_nope, const mla_bf16* q_rope,
+                                  const mla_bf16* W_UK, const int32_t* seqlens, mla_bf16* q_cat,
+                                  int B, int S, int H, const double* theta, void* stream) {
+  if (!q_rope || !seqlens || !aligned16(q_rope)) return MLA_ERR_INVALID_ARG;
+  mla::RopeTheta th;
+  if (!copy_theta(theta, &th)) return MLA_ERR_INVALID_ARG;
+  return absorb_launch(q_nope, q_rope, W_UK, seqlens, q_cat, B, S, H, th, stream);
+}
+
+int mla_rope_yarn_frequencies(double base, double s, double alpha, double beta, double orig_len,
+                              double* theta) {
+  if (!theta || !(base > 1.0) || !std::isfinite(base) || !(s >= 1.0) || !std::isfinite(s) ||
+      !(beta > alpha) || !std::isfinite(alpha) || !std::isfinite(beta) || !(orig_len > 0.0) ||
+      !std::isfinite(orig_len))
+    return MLA_ERR_INVALID_ARG;
+  const double two_pi = 6.283185307179586476925286766559;
+  for (int j = 0; j < 32; ++j) {
+    const double th = std::pow(base, -2.0 * j / 64.0);
+    // blend weight: 0 below alpha turns over the original context, 1 above beta
+    const double turns = orig_len * th / two_pi;
+    const double w = std::min(1.0, std::max(0.0, (turns - alpha) / (beta - alpha)));
+    theta[j] = w * th + (1.0 - w) * (th / s);
+  }
+  return MLA_OK;
+}
+
+mla_status mla_rope_apply(const mla_bf16* x_in, int64_t in_stride_n, int64_t in_stride_h,
+                          mla_bf16* x_out, int64_t out_stride_n, int64_t out_stride_h, int64_t N,
+                          int nh, int pos_mode, const int32_t* pos_src, int group, float base,
+                          void* stream) {
+  if (!(base > 1.0f) || !std::isfinite(base)) return MLA_ERR_INVALID_ARG;
+  return rope_launch(x_in, in_stride_n, in_stride_h, x_out, out_stride_n, out_stride_h, N, nh,
+                     pos_mode, pos_src, group, base_theta(base), stream);
+}
+
+mla_status mla_rope_apply_freq(const mla_bf16* x_in, int64_t in_stride_n, int64_t in_stride_h,
+                               mla_bf16* x_out, int64_t out_stride_n, int64_t out_stride_h,
+                               int64_t N, int nh, int pos_mode, const int32_t* pos_src, int group,
+                               const double* theta, void* stream) {
+  mla::RopeTheta th;
+  if (!copy_theta(theta, &th)) return MLA_ERR_INVALID_ARG;
+  return rope_launch(x_in, in_stride_n, in_stride_h, x_out, out_stride_n, out_stride_h, N, nh,
+                     pos_mode, pos_src, group, th, stream);
 }
 
 size_t mla_decode_workspace_size(int B, int S, int H) {
