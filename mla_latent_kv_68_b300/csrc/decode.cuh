@@ -22,7 +22,9 @@
 //       one box of four 128-row x 64-column blocks (one 128-byte-swizzle atom
 //       per block), and a k^R ring of 16 KB stages; a tile is two c stages and
 //       one k^R stage, and at a segment start the 128 query rows of q_cat pass
-//       through the same rings on their way into tensor memory.  Box size and
+//       through the same rings on their way into tensor memory (TMA boxes
+//       arrive well before row-wise loads, which wait behind the cache stream
+//       in L2).  Box size and
 //       count matter on B300: an SM's TMA unit handles only a few boxes per
 //       microsecond, so 16 KB boxes cap an SM near 50 GB/s, 32 KB boxes near
 //       65-95 GB/s and 64 KB boxes near 100-120 GB/s.
@@ -50,6 +52,18 @@
 // segment (a sequence's share of a group's run) leaves O unnormalised plus
 // (m, l) per row; splitkv.cuh merges them.
 //
+// Cold code.  The first pass through the softmax's exponent section (about
+// 6 KB of unrolled code) takes about 5 us: its instruction lines miss one
+// after another, in step on every SM, with or without the cache stream
+// running.  Run on the first tile, that sits on the path every later tile
+// waits on.  So it is run early, "dry", on a stand-in tile -- no waits, no
+// barrier arrivals, no global reads or writes, results discarded -- by the
+// warps that are otherwise idle then: in the score CTA the hf = 1 half of
+// the softmax warps (the hf = 0 half alone moves the first query rows into
+// tensor memory meanwhile), in the value CTA all row warps (their first P
+// arrives several microseconds later).  The dry visit needs nothing from the
+// kernels before this one, so it starts before the dependency wait.
+//
 // Every wait is bounded (sm100.cuh), including the exchanges between the two
 // threads of a row, which go through mbarriers rather than bar.sync.  A wait
 // that runs out aborts the CTA's remaining work; the cluster peer notices
@@ -69,11 +83,13 @@ constexpr int kBlk0 = kTok * 128;          // one block: 128 rows x 64 bf16 = 16
 constexpr int kCStage = 4 * kBlk0;         // c ring stage: four blocks (one 64 KB TMA box)
 constexpr int kCStages = 2;
 constexpr int kRStage = kBlk0;             // k^R ring stage: one block (16 KB)
-constexpr int kRStages = 3;
+constexpr int kRStages = 2;
 constexpr int kOffR = kCStages * kCStage;  // k^R ring
-constexpr int kOffPS = kOffR + kRStages * kRStage;  // P staging: 128 x 128 bf16 + rescale exponents[128]
+constexpr int kOffQR = kOffR + kRStages * kRStage;  // q^R of the segment: 128 x 64 bf16 (A of the RoPE MMAs)
+constexpr int kOffPS = kOffQR + kBlk0;     // P staging: 128 x 128 bf16 + rescale exponents[128] + row sums
 constexpr int kPBytes = 128 * kTok * 2;
-constexpr uint32_t kPTx = kPBytes + 128;      // bytes of one P slot with its exponent column
+constexpr int kOffPL = kPBytes + 128;         // in a P slot: row sums l (f32 [128]) after the exponents
+constexpr uint32_t kPTx = kOffPL + 512;       // bytes of one P slot: P, rescale exponents, row sums
 constexpr int kOffXch = kOffPS + (int)kPTx;   // ceil(row max) int16 [2 tiles][2 halves][128], row sum f32 [128]
 constexpr int kXchBytes = 2 * 2 * 128 * 2 + 128 * 4;
 // value CTA (rank 1)
@@ -87,21 +103,20 @@ constexpr int kPSlot = 33 * 1024;          // slot stride (keeps P 1 KB aligned)
 // shared by both
 constexpr int kEnd0 = kOffXch + kXchBytes, kEnd1 = kOffP + 2 * kPSlot;
 constexpr int kOffBar = kEnd0 > kEnd1 ? kEnd0 : kEnd1;
-constexpr int kNumBars = 46;
+constexpr int kNumBars = 48;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kDecSmem = kOffMisc + 16;
 static_assert(kDecSmem <= 232448, "decode shared memory exceeds 227 KB");
-static_assert(kOffPS % 1024 == 0 && kOffP % 1024 == 0 && kPSlot % 1024 == 0,
+static_assert(kOffQR % 1024 == 0 && kOffPS % 1024 == 0 && kOffP % 1024 == 0 && kPSlot % 1024 == 0,
               "swizzled operands need 1 KB alignment");
 static_assert(kPTx % 16 == 0 && kPTx <= (uint32_t)kPSlot,
               "P slot layout");
-constexpr uint32_t kQCol = 256;   // score CTA: q~ at tensor-memory columns 256..511
-constexpr uint32_t kQRCol = 128;  // score CTA: q^R at columns 128..159; S at 0..127
+constexpr uint32_t kQCol = 256;   // score CTA: q~ at tensor-memory columns 256..511; S buffers at 0, 128
 
 // barrier indices
 enum : int {
-  B_FULL = 0, B_EMPTY = 10,          // TMA rings (rank 0: c at 0..1, k^R at 2..4; rank 1: 0..1)
-  B_SFULL = 20, B_SEMPTY = 22,       // score CTA: S buffer (one; index 0 used)
+  B_FULL = 0, B_EMPTY = 10,          // TMA rings (rank 0: c at 0..1, k^R at 2..3; rank 1: 0..1)
+  B_SFULL = 20, B_SEMPTY = 22,       // score CTA: the two S buffers
   B_PEMPTY = 24,                     // score CTA: P slot in the value CTA free again
   B_QREADY = 26,                     // score CTA: Q of the segment is in place
   B_XCH = 27,                        // score CTA: row-max exchange [tile parity][quadrant]
@@ -112,7 +127,9 @@ enum : int {
   B_PREADY = 40,                     // value CTA: O rescaled, P may be consumed
   B_PVDONE = 42,                     // value CTA: P . C of a tile completed
   B_OFREE = 44,                      // value CTA: epilogue has read O
-  B_DRAIN = 45                       // both: final MMA drain
+  B_DRAIN = 45,                      // both: final MMA drain
+  B_QRFULL = 46,                     // score CTA: q^R of the segment has landed
+  B_QREMPTY = 47                     // score CTA: the segment's MMAs no longer read q^R
 };
 
 struct DecodeParams {
@@ -122,7 +139,7 @@ struct DecodeParams {
   const int32_t* segbase;
   const int32_t* gstart;       // [G] first sequence of each group's run
   float2* ml;                  // [slots * n_rb, 128]        (m, l) per row
-  float* opart;                // [slots * n_rb, 512, 128]   column-major O per segment
+  uint4* opart;                // [slots * n_rb][64 column octets][128 rows] fp16 x 8: O / l per segment
   uint32_t* status;
   const uint32_t* plan_ok;
   int B, S, H, Lmax, n_rb, G;
@@ -134,38 +151,98 @@ struct TileInfo {
   int b, t, L, i, k, slot;
   int nvt;  // cache rows of the sequence inside this tile (1..128)
   bool first, last;
+  bool dry;  // warm-up visit of a stand-in tile: compute only, no waits, no global reads or writes
 };
 
-// Visit, in order, every cache tile of group g (see splitkv.cuh for the plan).
+// Tiles of group g in order (see splitkv.cuh for the plan), as a cursor.
+struct TileCursor {
+  int64_t beg, end;  // the group's flat tiles [beg, end)
+  int g, b, t, tb, te, i, k, slot, L;
+};
+
+// Move c to the first sequence from c.b on that has tiles in the run.
+__device__ __forceinline__ bool cursor_seq(const DecodeParams& p, TileCursor& c) {
+  for (; c.b < p.B; ++c.b) {
+    const int64_t x0 = p.prefix[c.b], x1 = p.prefix[c.b + 1];
+    if (x0 >= c.end) return false;
+    if (x1 <= c.beg) continue;
+    c.tb = (int)(max(c.beg, x0) - x0);
+    c.te = (int)(min(c.end, x1) - x0);
+    c.t = c.tb;
+    c.slot = p.segbase[c.b] + (c.g - p.gfirst[c.b]);
+    c.L = p.seqlens[c.b];
+    return true;
+  }
+  return false;
+}
+
+__device__ __forceinline__ bool cursor_start(const DecodeParams& p, int g, TileCursor& c) {
+  const int64_t T = p.prefix[p.B];
+  if (T <= 0) return false;
+  c.beg = (int64_t)g * T / p.G;
+  c.end = (int64_t)(g + 1) * T / p.G;
+  if (c.beg >= c.end) return false;
+  c.g = g;
+  c.i = 0;
+  c.k = 0;
+  c.b = p.gstart[g];
+  return cursor_seq(p, c);
+}
+
+__device__ __forceinline__ bool cursor_next(const DecodeParams& p, TileCursor& c) {
+  ++c.i;
+  if (++c.t < c.te) return true;
+  ++c.k;
+  ++c.b;
+  return cursor_seq(p, c);
+}
+
+__device__ __forceinline__ TileInfo cursor_tile(const TileCursor& c) {
+  return TileInfo{c.b, c.t, c.L, c.i, c.k, c.slot, min(c.L - c.t * kTok, kTok), c.t == c.tb, c.t == c.te - 1,
+                  false};
+}
+
+// Visit every tile of group g in order.
 template <class F>
 __device__ __forceinline__ void for_each_tile(const DecodeParams& p, int g, F&& f) {
-  const int64_t T = p.prefix[p.B];
-  if (T <= 0) return;
-  const int64_t beg = (int64_t)g * T / p.G, end = (int64_t)(g + 1) * T / p.G;
-  if (beg >= end) return;
-  int i = 0, k = 0;
-  for (int b = p.gstart[g]; b < p.B; ++b) {
-    const int64_t x0 = p.prefix[b], x1 = p.prefix[b + 1];
-    if (x0 >= end) break;
-    if (x1 <= beg) continue;
-    const int tb = (int)(max(beg, x0) - x0), te = (int)(min(end, x1) - x0);
-    const int slot = p.segbase[b] + (g - p.gfirst[b]);
-    const int L = p.seqlens[b];
-    for (int t = tb; t < te; ++t, ++i) {
-      const TileInfo ti{b, t, L, i, k, slot, min(L - t * kTok, kTok), t == tb, t == te - 1};
-      if (!f(ti)) return;
+  TileCursor c;
+  for (bool have = cursor_start(p, g, c); have; have = cursor_next(p, c))
+    if (!f(cursor_tile(c))) return;
+}
+
+// The row warps' walk: optionally a dry visit of a stand-in tile first (no
+// plan or global data needed, so it runs before the kernels this one depends
+// on have finished), then the dependency wait, then every tile of group g.
+// All visits go through the same call of f so that they run the same code.
+template <class F>
+__device__ __forceinline__ void for_each_tile_warm(const DecodeParams& p, int g, const volatile uint32_t* abort_flag,
+                                                   bool dry_first, F&& f) {
+  TileInfo ti{0, 0, kTok, 0, 0, 0, kTok, true, false, true};
+  TileCursor c;
+  bool have = true;
+  if (!dry_first) {
+    pdl_wait();  // q_cat and the plan come from the kernels before this one
+    have = *p.plan_ok != 0u && *abort_flag == 0u && cursor_start(p, g, c);
+    if (have) ti = cursor_tile(c);
+  }
+  while (have) {
+    if (!f(ti)) return;
+    if (ti.dry) {
+      pdl_wait();
+      have = *p.plan_ok != 0u && *abort_flag == 0u && cursor_start(p, g, c);
+    } else {
+      have = cursor_next(p, c);
     }
-    ++k;
+    if (have) ti = cursor_tile(c);
   }
 }
 
-// Score-CTA ring positions for tile i of segment k.  Every segment first
-// sends its query rows through the rings (two c stages, one k^R stage),
-// every tile its cache rows (the same).  c stage h holds blocks 4h .. 4h + 3.
+// Score-CTA c-ring positions for tile i of segment k.  Every segment first
+// sends its 512 q~ columns through the c ring (two stages), every tile its
+// cache rows (the same); c stage h holds blocks 4h .. 4h + 3.  The k^R ring
+// carries cache rows only (tile i at position i); q^R has its own buffer.
 __device__ __forceinline__ int cpos_q(int i, int k, int h) { return 2 * (i + k) + h; }
 __device__ __forceinline__ int cpos_kv(int i, int k, int h) { return 2 * (i + k + 1) + h; }
-__device__ __forceinline__ int rpos_q(int i, int k) { return i + k; }
-__device__ __forceinline__ int rpos_kv(int i, int k) { return i + k + 1; }
 constexpr int kBarC = 0, kBarR = kCStages;  // FULL / EMPTY sub-ranges of the two rings
 
 // All 32 lanes wait; the outcome is made warp-uniform so that warp-collective
@@ -219,6 +296,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     mbar_init(&bar[B_PSFREE], 1);
     mbar_init(&bar[B_OFREE], 256);
     mbar_init(&bar[B_DRAIN], 1);
+    mbar_init(&bar[B_QRFULL], 1);
+    mbar_init(&bar[B_QREMPTY], 1);
     if (rank == 1) {  // first phase of each P slot expects one slot's bytes
       mbar_arrive_expect_tx(&bar[B_PFULL + 0], kPTx);
       mbar_arrive_expect_tx(&bar[B_PFULL + 1], kPTx);
@@ -242,15 +321,17 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   tc_fence_after();
   cluster_sync();  // the peer's barriers exist before anyone arrives on them remotely
   pdl_trigger();
-  pdl_wait();      // q_cat and the plan come from the kernels before this one
+  const bool rows = warp >= 4;
+  if (!rows) pdl_wait();  // q_cat and the plan come from the kernels before this one (row warps: later)
   const uint32_t tmem = *tmem_slot;
-  const bool run = (*p.plan_ok != 0u) && (*abort_flag == 0u);
+  const bool run = rows || ((*p.plan_ok != 0u) && (*abort_flag == 0u));
 
   if (run && warp == 0) {
     // ------------------------------------------------ TMA producer (both CTAs)
     if (lane == 0) {
       int last_use[kCStages + kRStages];
       for (int s = 0; s < kCStages + kRStages; ++s) last_use[s] = -1;
+      int qr_last = -1;  // last segment whose q^R was loaded
       int cq = 0, rq = 0, q = 0;  // running positions: score c ring, score k^R ring, value ring
       // Issue one stage of a ring: wait for the slot, arm its barrier, copy.
       auto slot = [&](int base, int nst, int pos, uint32_t bytes) -> int {
@@ -263,16 +344,17 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       for_each_tile(p, g, [&](const TileInfo& ti) {
         const int row0 = ti.b * p.Lmax + ti.t * kTok;
         if (rank == 0) {
-          if (ti.first) {  // the segment's query rows: blocks 0..7 through the c ring, q^R through k^R's
+          if (ti.first) {  // the segment's query rows: blocks 0..7 through the c ring, q^R to its buffer
             const int qrow0 = ti.b * SH + rb * 128;
             for (int h = 0; h < 2; ++h, ++cq) {
               const int st = slot(kBarC, kCStages, cq, kCStage);
               if (st < 0) return false;
               tma_load_3d(smem + st * kCStage, &tm_q, &bar[B_FULL + kBarC + st], 0, qrow0, 4 * h);
             }
-            const int st = slot(kBarR, kRStages, rq++, kRStage);
-            if (st < 0) return false;
-            tma_load_2d(smem + kOffR + st * kRStage, &tm_qr, &bar[B_FULL + kBarR + st], 512, qrow0);
+            if (!mbar_wait(&bar[B_QREMPTY], ((uint32_t)ti.k & 1u) ^ 1u, wc)) return false;
+            mbar_arrive_expect_tx(&bar[B_QRFULL], kBlk0);
+            qr_last = ti.k;
+            tma_load_2d(smem + kOffQR, &tm_qr, &bar[B_QRFULL], 512, qrow0);
           }
           for (int h = 0; h < 2; ++h, ++cq) {
             const int st = slot(kBarC, kCStages, cq, kCStage);
@@ -298,6 +380,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         const int nst = rank == 0 ? (s < kBarR ? kCStages : kRStages) : kStages1;
         mbar_wait_drain(&bar[B_FULL + s], (uint32_t)(last_use[s] / nst) & 1u, wc);
       }
+      if (qr_last >= 0) mbar_wait_drain(&bar[B_QRFULL], (uint32_t)qr_last & 1u, wc);
     }
   } else if (run && warp == 1) {
     // ------------------------------------------------ MMA issuer (one thread)
@@ -305,14 +388,15 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       if (rank == 0) {
         constexpr uint32_t idesc = idesc_bf16_f32(128, kTok, 0, 0);
         for_each_tile(p, g, [&](const TileInfo& ti) {
-          const uint32_t sph = (uint32_t)ti.i & 1u;  // the single S buffer, one phase per tile
-          if (ti.first) {  // the query stages have been moved out of the rings: release them
+          const int sb = ti.i & 1;                            // S buffer of this tile
+          const uint32_t sph = (uint32_t)(ti.i >> 1) & 1u;    // its phase
+          if (ti.first) {  // q~ has been moved out of the c ring: release it; q^R must have landed
             if (!mbar_wait(&bar[B_QREADY], (uint32_t)ti.k & 1u, wc)) return false;
             for (int h = 0; h < 2; ++h) mbar_arrive(&bar[B_EMPTY + kBarC + cpos_q(ti.i, ti.k, h) % kCStages]);
-            mbar_arrive(&bar[B_EMPTY + kBarR + rpos_q(ti.i, ti.k) % kRStages]);
+            if (!mbar_wait(&bar[B_QRFULL], (uint32_t)ti.k & 1u, wc)) return false;
           }
-          if (!mbar_wait(&bar[B_SEMPTY], sph ^ 1u, wc)) return false;
-          const uint32_t d = tmem;
+          if (!mbar_wait(&bar[B_SEMPTY + sb], sph ^ 1u, wc)) return false;
+          const uint32_t d = tmem + (uint32_t)sb * 128u;
           for (int h = 0; h < 2; ++h) {  // c blocks 4h .. 4h + 3 against q~ from tensor memory
             const int q = cpos_kv(ti.i, ti.k, h), st = q % kCStages;
             if (!mbar_wait(&bar[B_FULL + kBarC + st], (uint32_t)(q / kCStages) & 1u, wc)) return false;
@@ -326,17 +410,18 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             }
             mma_commit(&bar[B_EMPTY + kBarC + st]);
           }
-          {  // k^R against q^R, both 64 wide
-            const int q = rpos_kv(ti.i, ti.k), st = q % kRStages;
+          {  // k^R against q^R, both 64 wide and K-major in shared memory
+            const int q = ti.i, st = q % kRStages;
             if (!mbar_wait(&bar[B_FULL + kBarR + st], (uint32_t)(q / kRStages) & 1u, wc)) return false;
             tc_fence_after();
-            const uint32_t sbase = smem_u32(smem + kOffR + st * kRStage);
+            const uint32_t sbase = smem_u32(smem + kOffR + st * kRStage), qbase = smem_u32(smem + kOffQR);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              mma_ts(d, tmem + kQRCol + (uint32_t)kk * 8, smem_desc(sbase + kk * 32, 16, 1024, 2), idesc, 1u);
+              mma_ss(d, smem_desc(qbase + kk * 32, 16, 1024, 2), smem_desc(sbase + kk * 32, 16, 1024, 2), idesc, 1u);
             mma_commit(&bar[B_EMPTY + kBarR + st]);
           }
-          mma_commit(&bar[B_SFULL]);
+          if (ti.last) mma_commit(&bar[B_QREMPTY]);  // the buffer may take the next segment's q^R
+          mma_commit(&bar[B_SFULL + sb]);
           return true;
         });
       } else {
@@ -419,23 +504,20 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       uint8_t* ps = smem + kOffPS;
       float m_ref = -INFINITY, l = 0.f;
       int limit = 0;
-      for_each_tile(p, g, [&](const TileInfo& ti) {
+      for_each_tile_warm(p, g, abort_flag, /*dry_first=*/hf == 1, [&](const TileInfo& ti) {
         if (ti.first) {
-          // q~ into tensor memory (this thread: 4 of its row's 8 blocks), q^R
-          // into its own buffer; the blocks come through the ring.
           limit = valid ? ti.L - p.S + s_r + 1 : 0;
-          for (int j = hf * 4; j < hf * 4 + 4 + hf; ++j) {  // block j of the query row
-            const uint8_t* rowp;
-            if (j < 8) {  // c stage hf, block j - 4 hf
-              const int q = cpos_q(ti.i, ti.k, hf), st = q % kCStages;
+          // q~ into tensor memory (block j at columns kQCol + 32 j); the
+          // blocks come through the c ring.  The group's first query rows are
+          // moved by the hf = 0 thread alone (its partner is in the dry visit
+          // then), later ones by both, four blocks each.
+          const bool whole = ti.i == 0;
+          if (!ti.dry && (!whole || hf == 0)) {
+            const int j0 = whole ? 0 : hf * 4, j1 = whole ? 8 : hf * 4 + 4;
+            for (int j = j0; j < j1; ++j) {
+              const int q = cpos_q(ti.i, ti.k, j >> 2), st = q % kCStages;
               if (!warp_wait(&bar[B_FULL + kBarC + st], (uint32_t)(q / kCStages) & 1u, wc)) return false;
-              rowp = smem + st * kCStage + (j - 4 * hf) * kBlk0 + r * 128;
-            } else {      // q^R through the k^R ring
-              const int q = rpos_q(ti.i, ti.k), st = q % kRStages;
-              if (!warp_wait(&bar[B_FULL + kBarR + st], (uint32_t)(q / kRStages) & 1u, wc)) return false;
-              rowp = smem + kOffR + st * kRStage + r * 128;
-            }
-            if (j < 8) {
+              const uint8_t* rowp = smem + st * kCStage + (j & 3) * kBlk0 + r * 128;
               uint32_t v[32];
 #pragma unroll
               for (int ch = 0; ch < 8; ++ch) {  // logical chunk ch sits at ch ^ (r & 7)
@@ -443,42 +525,35 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                 v[4 * ch] = x.x; v[4 * ch + 1] = x.y; v[4 * ch + 2] = x.z; v[4 * ch + 3] = x.w;
               }
               tmem_st32(tl + kQCol + (uint32_t)j * 32, v);
-            } else {  // q^R: 32 tensor-memory columns
-              uint32_t v[32];
-#pragma unroll
-              for (int ch = 0; ch < 8; ++ch) {
-                const uint4 x = *reinterpret_cast<const uint4*>(rowp + ((ch ^ (r & 7)) << 4));
-                v[4 * ch] = x.x; v[4 * ch + 1] = x.y; v[4 * ch + 2] = x.z; v[4 * ch + 3] = x.w;
-              }
-              tmem_st32(tl + kQRCol, v);
             }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive_n(&bar[B_QREADY], whole ? 2u : 1u);
           }
-          tmem_wait_st();
-          tc_fence_before();
-          mbar_arrive(&bar[B_QREADY]);
           m_ref = -INFINITY;
           l = 0.f;
         }
-        const int slot = ti.i & 1;
+        const int slot = ti.i & 1;  // S buffer and exchange slot of this tile
         const uint32_t sph = (uint32_t)(ti.i >> 1) & 1u;
-        if (!warp_wait(&bar[B_SFULL], (uint32_t)ti.i & 1u, wc)) return false;
+        if (!ti.dry && !warp_wait(&bar[B_SFULL + slot], sph, wc)) return false;
         tc_fence_after();
-        uint32_t sv[64];
-        {
-          uint32_t (&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[0]);
-          uint32_t (&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[32]);
-          tmem_ld32(tl + (uint32_t)(hf * 64), lo);
-          tmem_ld32(tl + (uint32_t)(hf * 64 + 32), hi);
-        }
-        tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(&bar[B_SEMPTY]);
-
+        const uint32_t sc = tl + (uint32_t)(slot * 128 + hf * 64);  // this thread's 64 score columns
         const int nv = min(max(limit - ti.t * kTok - hf * 64, 0), 64);
+
+        // The scores are read from tensor memory twice, 16 at a time, in
+        // rolled loops: the code stays small (its first run is bound by
+        // instruction fetch), and the other S buffer lets the next tile's
+        // QK^T run meanwhile.
         float mx = -INFINITY;  // max of the raw scores; the scale is positive
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[16];
+          tmem_ld16(sc + (uint32_t)(c * 16), v);
+          tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < 64; ++c)
-          if (c < nv) mx = fmaxf(mx, __uint_as_float(sv[c]));
+          for (int u = 0; u < 16; ++u)
+            if (c * 16 + u < nv) mx = fmaxf(mx, __uint_as_float(v[u]));
+        }
         mx *= p.scale_log2;
         // Both threads of the row (same quadrant, warps q4 and q4 + 4) need the
         // same new reference exponent, which depends on the row maximum only
@@ -486,8 +561,10 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         // So the two halves exchange ceil(max) as a 16-bit integer.
         const int cm = mx == -INFINITY ? -32768 : (int)fminf(fmaxf(ceilf(mx), -32000.f), 32000.f);
         xch[(slot * 2 + hf) * 128 + r] = (int16_t)cm;
-        mbar_arrive(&bar[B_XCH + slot * 4 + q4]);
-        if (!warp_wait(&bar[B_XCH + slot * 4 + q4], sph, wc)) return false;
+        if (!ti.dry) {
+          mbar_arrive(&bar[B_XCH + slot * 4 + q4]);
+          if (!warp_wait(&bar[B_XCH + slot * 4 + q4], sph, wc)) return false;
+        }
         const int cmax = max(cm, (int)xch[(slot * 2 + (hf ^ 1)) * 128 + r]);
         int ex = 0;  // rescale 2^-ex of O and l; 255 stands for 0
         if (cmax > -32768 && (float)cmax > m_ref + 8.f) {
@@ -497,55 +574,71 @@ __global__ void __launch_bounds__(kDecThreads, 1)
           m_ref = mn;
         }
         const float mu = (m_ref == -INFINITY) ? 0.f : m_ref;
-        uint32_t pk[32];
-        float lsum0 = 0.f, lsum1 = 0.f;
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {  // 2^(s * scale * log2 e - m)
-          const float e0 = (2 * c < nv) ? ex2_approx(fmaf(__uint_as_float(sv[2 * c]), p.scale_log2, -mu)) : 0.f;
-          const float e1 =
-              (2 * c + 1 < nv) ? ex2_approx(fmaf(__uint_as_float(sv[2 * c + 1]), p.scale_log2, -mu)) : 0.f;
-          pk[c] = pack_bf16x2(e0, e1);
-          const __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162*>(&pk[c]);
-          lsum0 += __low2float(b2);
-          lsum1 += __high2float(b2);
-        }
-        l += lsum0 + lsum1;
 
         // the staging buffer is free once the previous tile's copy has read it
-        if (!warp_wait(&bar[B_PSFREE], ((uint32_t)ti.i & 1u) ^ 1u, wc)) return false;
+        if (!ti.dry && !warp_wait(&bar[B_PSFREE], ((uint32_t)ti.i & 1u) ^ 1u, wc)) return false;
         uint8_t* row = ps + hf * 16384 + r * 128;
+        float lsum0 = 0.f, lsum1 = 0.f;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {  // 2^(s * scale * log2 e - m) for 16 columns: two 16-byte chunks of P
+          uint32_t v[16];
+          tmem_ld16(sc + (uint32_t)(c * 16), v);
+          tmem_wait_ld();
+          uint32_t pk[8];
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch)  // 128-byte swizzle: chunk ch of row r sits at ch ^ (r & 7)
-          *reinterpret_cast<uint4*>(row + ((ch ^ (r & 7)) << 4)) =
-              make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-        if (hf == 0) ps[kPBytes + r] = (uint8_t)ex;
-        fence_proxy_async_cta();  // the bulk copy reads the buffer through the async proxy
-        mbar_arrive(&bar[B_PSTAGED]);
-        if (ti.last) {  // segment end: add the two halves' sums, write (m, l)
+          for (int u = 0; u < 8; ++u) {
+            const int col = c * 16 + 2 * u;
+            const float e0 = col < nv ? ex2_approx(fmaf(__uint_as_float(v[2 * u]), p.scale_log2, -mu)) : 0.f;
+            const float e1 =
+                col + 1 < nv ? ex2_approx(fmaf(__uint_as_float(v[2 * u + 1]), p.scale_log2, -mu)) : 0.f;
+            pk[u] = pack_bf16x2(e0, e1);
+            const __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162*>(&pk[u]);
+            lsum0 += __low2float(b2);
+            lsum1 += __high2float(b2);
+          }
+          // 128-byte swizzle: chunk ch of row r sits at ch ^ (r & 7)
+          *reinterpret_cast<uint4*>(row + (((2 * c) ^ (r & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          *reinterpret_cast<uint4*>(row + (((2 * c + 1) ^ (r & 7)) << 4)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        }
+        tc_fence_before();
+        if (!ti.dry) mbar_arrive(&bar[B_SEMPTY + slot]);  // this S buffer has been read
+        l += lsum0 + lsum1;
+        float l_seg = 0.f;  // segment end: the row's whole sum (both halves), for hf = 0
+        if (ti.last && !ti.dry) {
           if (hf == 1) xl[r] = l;
           mbar_arrive(&bar[B_XL]);
           if (!warp_wait(&bar[B_XL], (uint32_t)ti.k & 1u, wc)) return false;
-          if (hf == 0 && valid)
-            p.ml[((size_t)ti.slot * p.n_rb + rb) * 128 + r] = make_float2(mu, l + xl[r]);
+          l_seg = l + xl[r];
           // the next segment's exchange reuses xl only after its own tiles'
           // row-max exchanges, which both threads pass after reading it here
         }
+        if (hf == 0) {
+          ps[kPBytes + r] = (uint8_t)ex;
+          reinterpret_cast<float*>(ps + kOffPL)[r] = l_seg;  // the value CTA normalises O with it
+        }
+        fence_proxy_async_cta();  // the bulk copy reads the buffer through the async proxy
+        if (ti.dry) return true;
+        mbar_arrive(&bar[B_PSTAGED]);
+        if (ti.last && hf == 0 && valid)  // segment end: (m, l) of the row
+          p.ml[((size_t)ti.slot * p.n_rb + rb) * 128 + r] = make_float2(mu, l_seg);
         return true;
       });
     } else {
       // ---------------------------------------- rescale, tail zeroing, epilogue
       const int wt = threadIdx.x - 128;  // 0..255
       int q = 0;  // running stage counter (as the producer's)
-      for_each_tile(p, g, [&](const TileInfo& ti) {
+      for_each_tile_warm(p, g, abort_flag, /*dry_first=*/true, [&](const TileInfo& ti) {
         const int slot = ti.i & 1;
         const uint32_t sph = (uint32_t)(ti.i >> 1) & 1u;
         const int nsub = (ti.nvt + kSub - 1) / kSub;
         const int q0 = q;
-        q += nsub;
-        if (!warp_wait(&bar[B_PFULL + slot], sph, wc)) return false;
+        if (!ti.dry) q += nsub;
+        if (!ti.dry && !warp_wait(&bar[B_PFULL + slot], sph, wc)) return false;
         const int ex = reinterpret_cast<const volatile uint8_t*>(smem + kOffP + slot * kPSlot + kPBytes)[r];
+        const float l_seg = ti.last
+            ? reinterpret_cast<const volatile float*>(smem + kOffP + slot * kPSlot + kOffPL)[r] : 0.f;
         const float alpha = ex == 255 ? 0.f : exp2_int(-ex);
-        if (wt == 0) mbar_arrive_expect_tx(&bar[B_PFULL + slot], kPTx);  // arm the slot's next phase
+        if (!ti.dry && wt == 0) mbar_arrive_expect_tx(&bar[B_PFULL + slot], kPTx);  // arm the slot's next phase
         const bool need = !ti.first && alpha != 1.f;
         if (__any_sync(0xffffffffu, need)) {
           // O rows change only after the previous tile's P . C has completed
@@ -565,6 +658,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
           }
           tmem_wait_st();
         }
+        if (ti.dry) return true;
         if (ti.nvt & 15) {
           // cache rows past the sequence end inside the last 16-row MMA step hold
           // arbitrary bytes; their weights are 0 but 0 * NaN is not, so zero them
@@ -584,10 +678,13 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         if (ti.last) {
           if (!warp_wait(&bar[B_PVDONE + slot], sph, wc)) return false;
           tc_fence_after();
-          // O partial, column-major [512][128] f32: for each column a warp
-          // stores 32 consecutive floats.  Two 32-column loads per wait keep
-          // more stores in flight.
-          float* dst = p.opart + ((size_t)ti.slot * p.n_rb + rb) * 512 * 128 + r;
+          // O / l in fp16 as [64 column octets][128 rows] of 16 bytes: each
+          // store of a warp covers 32 consecutive rows, 512 contiguous bytes.
+          // The epilogue is bound by an SM's store bandwidth, so halving the
+          // bytes (against fp32 O) halves its time; normalising first keeps
+          // the values within fp16 range (a convex mix of cache rows).
+          const float inv = l_seg > 0.f ? 1.f / l_seg : 0.f;
+          uint4* dst = p.opart + ((size_t)ti.slot * p.n_rb + rb) * 64 * 128 + r;
 #pragma unroll 1
           for (int c = 0; c < 4; ++c) {
             uint32_t v[64];
@@ -599,7 +696,12 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             }
             tmem_wait_ld();
 #pragma unroll
-            for (int u = 0; u < 64; ++u) dst[(size_t)(hf * 256 + c * 64 + u) * 128] = __uint_as_float(v[u]);
+            for (int u = 0; u < 8; ++u) {
+              const float* f = reinterpret_cast<const float*>(&v[8 * u]);
+              dst[(size_t)(hf * 32 + c * 8 + u) * 128] =
+                  make_uint4(pack_f16x2_sat(f[0] * inv, f[1] * inv), pack_f16x2_sat(f[2] * inv, f[3] * inv),
+                             pack_f16x2_sat(f[4] * inv, f[5] * inv), pack_f16x2_sat(f[6] * inv, f[7] * inv));
+            }
           }
           tc_fence_before();
           mbar_arrive(&bar[B_OFREE]);

@@ -99,8 +99,9 @@ bool encode_tiled(CUtensorMap* map, const void* base, cuuint32_t rank, const cuu
 }
 
 // Tensor maps of the decode kernel: the score CTA reads 128-row boxes of c
-// and k^R, the value CTA 32-row boxes of c (64 columns = 128 bytes each, the
-// width of one 128-byte-swizzle atom).
+// and q_cat (four 64-column blocks) and of k^R and q^R, the value CTA 64-row
+// boxes of c (all eight blocks); a block is 64 columns = 128 bytes, one
+// 128-byte-swizzle atom.
 struct DecodeMaps {
   CUtensorMap c0, kr, q, qr, c1;
 };
@@ -143,7 +144,7 @@ WsLayout ws_layout(int B, int S, int H, int max_clusters) {
   w.segbase = off; off = align256(off + sizeof(int32_t) * (B + 1));
   w.gstart = off;  off = align256(off + sizeof(int32_t) * w.G);
   w.ml = off;      off = align256(off + sizeof(float) * 2 * (size_t)w.slots * w.n_rb * 128);
-  w.opart = off;   off = align256(off + sizeof(float) * (size_t)w.slots * w.n_rb * 128 * 512);
+  w.opart = off;   off = align256(off + sizeof(uint16_t) * (size_t)w.slots * w.n_rb * 128 * 512);
   w.total = off;
   return w;
 }
@@ -411,7 +412,7 @@ mla_status mla_decode(const mla_bf16* q_cat, const mla_bf16* c_kv, const mla_bf1
   p.segbase = pp.segbase;
   p.gstart = pp.gstart;
   p.ml = reinterpret_cast<float2*>(ws + w.ml);
-  p.opart = reinterpret_cast<float*>(ws + w.opart);
+  p.opart = reinterpret_cast<uint4*>(ws + w.opart);
   p.status = pp.status;
   p.plan_ok = pp.plan_ok;
   p.B = B;
@@ -444,7 +445,7 @@ mla_status mla_splitkv_combine(const void* workspace, size_t workspace_bytes, ml
   p.gfirst = reinterpret_cast<const int32_t*>(ws + w.gfirst);
   p.segbase = reinterpret_cast<const int32_t*>(ws + w.segbase);
   p.ml = reinterpret_cast<const float2*>(ws + w.ml);
-  p.opart = reinterpret_cast<const float*>(ws + w.opart);
+  p.opart = reinterpret_cast<const uint4*>(ws + w.opart);
   p.o_lat = reinterpret_cast<__nv_bfloat16*>(o_lat);
   p.plan_ok = reinterpret_cast<const uint32_t*>(ws) + 1;
   p.B = B;
@@ -591,7 +592,7 @@ extern "C" mla_status mla_decode_noalloc(const mla_bf16* q_cat, const mla_bf16* 
   p.segbase = pp.segbase;
   p.gstart = pp.gstart;
   p.ml = reinterpret_cast<float2*>(ws + w.ml);
-  p.opart = reinterpret_cast<float*>(ws + w.opart);
+  p.opart = reinterpret_cast<uint4*>(ws + w.opart);
   p.status = status;
   p.plan_ok = plan_ok;
   p.B = B;

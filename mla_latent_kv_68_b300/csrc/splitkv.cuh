@@ -4,10 +4,11 @@
 // Attention / 注意力计算" normalises once over all visible positions.  The
 // decode kernel cuts every sequence's cache rows into contiguous runs of
 // 128-row tiles ("segments") spread over all SMs; each segment k leaves, per
-// query row, an unnormalised latent sum O_k = sum_j 2^(s2_j - m_k) c_j, its
-// reference exponent m_k (an integer, log2 units) and l_k = sum_j 2^(s2_j - m_k).
-// Merging them restores the single normalisation exactly:
-//     o_lat = sum_k 2^(m_k - M) O_k / sum_k 2^(m_k - M) l_k,   M = max_k m_k.
+// query row, its reference exponent m_k (an integer, log2 units), the sum
+// l_k = sum_j 2^(s2_j - m_k) and the normalised latent mix
+// U_k = sum_j 2^(s2_j - m_k) c_j / l_k (fp16).  Merging them restores the
+// single normalisation:
+//     o_lat = sum_k w_k U_k / sum_k w_k,   w_k = 2^(m_k - M) l_k,   M = max_k m_k.
 //
 // Tiles are kTileRows = 128 cache rows (the N of the decode's QK^T MMAs).
 // Plan: the cache tiles of all sequences are laid end to end (sequence-major)
@@ -137,7 +138,7 @@ struct CombineParams {
   const int32_t* gfirst;
   const int32_t* segbase;
   const float2* ml;     // [slots * n_rb, 128] (m_k, l_k)
-  const float* opart;   // [slots * n_rb, 512, 128] column-major
+  const uint4* opart;   // [slots * n_rb][64 column octets][128 rows] fp16 x 8 (U_k)
   __nv_bfloat16* o_lat; // [B*S*H, 512]
   const uint32_t* plan_ok;
   int B, S, H, n_rb, G;
@@ -152,10 +153,10 @@ __device__ __forceinline__ bool group_empty(int g, int64_t T, int G) {
 }
 
 // Block = one 128-row block of one sequence and kCombineCols latent columns;
-// thread = one query row.  Partials are column-major, so every load of a warp
-// reads 32 consecutive floats.  The (m, l) of all segments are read first;
-// the partial columns of two segments are then loaded together so that the
-// few L2 round trips of a row overlap.
+// thread = one query row.  Partials are stored as column octets x rows of
+// 8 fp16, so every 16-byte load of a warp reads 512 consecutive bytes.  The
+// (m, l) of all segments are read first; the partial columns of two segments
+// are then loaded together so that the few L2 round trips of a row overlap.
 constexpr int kCombineCols = 32;
 
 __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
@@ -182,7 +183,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
   float den = 0.f;
   for (int k = k0; k < k1; k += 2) {
     float w[2];
-    const float* src[2];
+    const uint4* src[2];
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
       const int kk = k + u;
@@ -192,19 +193,30 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
         const size_t idx = (size_t)kk * p.n_rb + rb;
         const float2 v = p.ml[idx * 128 + r];
         if (v.y > 0.f) {
-          w[u] = exp2f(v.x - M);
-          den += w[u] * v.y;
-          src[u] = p.opart + (idx * 512 + c0) * 128 + r;
+          w[u] = exp2f(v.x - M) * v.y;
+          den += w[u];
+          src[u] = p.opart + (idx * 64 + c0 / 8) * 128 + r;
         }
       }
     }
-    float x[2][kCombineCols];
+    uint4 x[2][kCombineCols / 8];
 #pragma unroll
     for (int u = 0; u < 2; ++u)
 #pragma unroll
-      for (int c = 0; c < kCombineCols; ++c) x[u][c] = w[u] != 0.f ? __ldg(src[u] + (size_t)c * 128) : 0.f;
+      for (int c = 0; c < kCombineCols / 8; ++c)
+        x[u][c] = w[u] != 0.f ? __ldg(src[u] + (size_t)c * 128) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-    for (int c = 0; c < kCombineCols; ++c) acc[c] += w[0] * x[0][c] + w[1] * x[1][c];
+    for (int c = 0; c < kCombineCols / 8; ++c) {
+      const uint32_t* a = reinterpret_cast<const uint32_t*>(&x[0][c]);
+      const uint32_t* b = reinterpret_cast<const uint32_t*>(&x[1][c]);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 fa = __half22float2(*reinterpret_cast<const __half2*>(&a[e]));
+        const float2 fb = __half22float2(*reinterpret_cast<const __half2*>(&b[e]));
+        acc[8 * c + 2 * e] += w[0] * fa.x + w[1] * fb.x;
+        acc[8 * c + 2 * e + 1] += w[0] * fa.y + w[1] * fb.y;
+      }
+    }
   }
   const float inv = den > 0.f ? 1.f / den : 0.f;
   uint4* dst = reinterpret_cast<uint4*>(p.o_lat + ((size_t)b * SH + rb * 128 + r) * 512 + c0);
