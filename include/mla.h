@@ -155,7 +155,7 @@ int mla_rope_yarn_frequencies(double base, double s, double alpha, double beta, 
  * Bytes of device workspace mla_decode needs for this shape on the current
  * device (it depends on the device's SM count).  0 if the shape is
  * unsupported or no device is present.  The workspace carries the device
- * status word, the split plan and the fp32 partial results that
+ * status word, the split plan and the partial results that
  * mla_splitkv_combine reads.
  */
 size_t mla_decode_workspace_size(int B, int S, int H);
@@ -166,8 +166,10 @@ size_t mla_decode_workspace_size(int B, int S, int H);
  *   s_j = (q_cat[..,0:512] . c_KV[b,j] + q_cat[..,512:576] . k_R[b,j]) * softmax_scale
  *   o_lat = sum_j softmax(s)_j c_KV[b,j]      (j = 0 .. L_b - S + s)
  * The cache rows of a sequence are split over all SMs (split-KV); each split
- * leaves an fp32 partial result and its log-sum-exp in the workspace, to be
- * merged by mla_splitkv_combine (call it next, with the same workspace).
+ * k leaves in the workspace, per query row, its reference exponent m_k, its
+ * weight sum l_k and its normalised latent mix U_k (fp16; values beyond the
+ * fp16 range saturate), to be merged by mla_splitkv_combine (call it next,
+ * with the same workspace).  The kernel works out the split plan itself.
  *   q_cat   [B,S,H,576]  bf16, absorbed + rotated queries
  *   c_kv    [B,Lmax,512] bf16 latent cache
  *   k_r     [B,Lmax,64]  bf16 rotated RoPE keys
@@ -183,7 +185,7 @@ mla_status mla_decode(const mla_bf16 *q_cat, const mla_bf16 *c_kv, const mla_bf1
 
 /*
  * Merge the split-KV partials left by mla_decode in `workspace`:
- *   o_lat = sum_k 2^(lse_k - M) O_k / sum_k 2^(lse_k - M),  M = max_k lse_k
+ *   o_lat = sum_k w_k U_k / sum_k w_k,  w_k = l_k 2^(m_k - M),  M = max_k m_k
  * which restores the single normalisation over all visible positions.
  *   o_lat [B,S,H,512] bf16 output.  B, S, H must match the mla_decode call.
  */

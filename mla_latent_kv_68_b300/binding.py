@@ -309,4 +309,4 @@ class DecodeStep:
             fn(*args, **kwargs)
         return g
 
-    LAUNCHES_PER_STEP = 5  # absorb + rope, plan, decode, combine, up-projection
+    LAUNCHES_PER_STEP = 4  # absorb + rope, decode (plans its own split), combine, up-projection

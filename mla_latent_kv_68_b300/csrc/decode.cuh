@@ -14,17 +14,20 @@
 // from N = 128 up (N = 64 reaches about half of it), so both contractions use
 // N >= 128.  The fp32 accumulator O (128 x 512) fills one SM's whole tensor
 // memory, so each unit of work is a CLUSTER OF TWO CTAs on two SMs:
-//   rank 0 ("score CTA"): q~ (128 x 512 bf16) and q^R (128 x 64) live in its
-//       tensor memory as the A operand of the QK^T MMAs (A-from-TMEM form),
-//       next to one 128-column S buffer; shared memory is left to the TMA
-//       ring, whose depth sets how many bytes an SM keeps in flight.
+//   rank 0 ("score CTA"): q~ (128 x 512 bf16) lives in its tensor memory as
+//       the A operand of the QK^T MMAs (A-from-TMEM form), next to two
+//       128-column S buffers (the MMAs of tile i+1 fill one while the softmax
+//       reads tile i from the other); q^R (128 x 64) sits in shared memory.
+//       Shared memory is otherwise left to the TMA rings, whose depth sets
+//       how many bytes an SM keeps in flight.
 //       Operands arrive through two TMA rings: a c ring of 64 KB stages, each
 //       one box of four 128-row x 64-column blocks (one 128-byte-swizzle atom
 //       per block), and a k^R ring of 16 KB stages; a tile is two c stages and
-//       one k^R stage, and at a segment start the 128 query rows of q_cat pass
-//       through the same rings on their way into tensor memory (TMA boxes
-//       arrive well before row-wise loads, which wait behind the cache stream
-//       in L2).  Box size and
+//       one k^R stage.  At a segment start the 512 q~ columns of the 128
+//       query rows pass through the c ring (two stages) and the MMA thread
+//       moves them into tensor memory with tcgen05.cp (TMA boxes arrive well
+//       before row-wise loads, which wait behind the cache stream in L2);
+//       q^R goes to a buffer of its own.  Box size and
 //       count matter on B300: an SM's TMA unit handles only a few boxes per
 //       microsecond, so 16 KB boxes cap an SM near 50 GB/s, 32 KB boxes near
 //       65-95 GB/s and 64 KB boxes near 100-120 GB/s.
@@ -58,11 +61,11 @@
 // running.  Run on the first tile, that sits on the path every later tile
 // waits on.  So it is run early, "dry", on a stand-in tile -- no waits, no
 // barrier arrivals, no global reads or writes, results discarded -- by the
-// warps that are otherwise idle then: in the score CTA the hf = 1 half of
-// the softmax warps (the hf = 0 half alone moves the first query rows into
-// tensor memory meanwhile), in the value CTA all row warps (their first P
-// arrives several microseconds later).  The dry visit needs nothing from the
-// kernels before this one, so it starts before the dependency wait.
+// row warps of both CTAs, which are idle then (the first scores and the
+// first P arrive several microseconds later).  The dry visit needs nothing
+// from the kernels before this one, so it starts before the dependency wait.
+// (The softmax is also written as rolled loops over 16-column slices, which
+// keeps that first pass short.)
 //
 // Every wait is bounded (sm100.cuh), including the exchanges between the two
 // threads of a row, which go through mbarriers rather than bar.sync.  A wait
@@ -103,9 +106,10 @@ constexpr int kPSlot = 33 * 1024;          // slot stride (keeps P 1 KB aligned)
 // shared by both
 constexpr int kEnd0 = kOffXch + kXchBytes, kEnd1 = kOffP + 2 * kPSlot;
 constexpr int kOffBar = kEnd0 > kEnd1 ? kEnd0 : kEnd1;
-constexpr int kNumBars = 48;
-constexpr int kOffMisc = kOffBar + kNumBars * 8;
-constexpr int kDecSmem = kOffMisc + 16;
+constexpr int kNumBars = 49;
+constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tensor-memory address, abort flag
+constexpr int kOffPlan = kOffMisc + 16;            // PlanState
+constexpr int kDecSmem = kOffPlan + 32;
 static_assert(kDecSmem <= 232448, "decode shared memory exceeds 227 KB");
 static_assert(kOffQR % 1024 == 0 && kOffPS % 1024 == 0 && kOffP % 1024 == 0 && kPSlot % 1024 == 0,
               "swizzled operands need 1 KB alignment");
@@ -118,7 +122,6 @@ enum : int {
   B_FULL = 0, B_EMPTY = 10,          // TMA rings (rank 0: c at 0..1, k^R at 2..3; rank 1: 0..1)
   B_SFULL = 20, B_SEMPTY = 22,       // score CTA: the two S buffers
   B_PEMPTY = 24,                     // score CTA: P slot in the value CTA free again
-  B_QREADY = 26,                     // score CTA: Q of the segment is in place
   B_XCH = 27,                        // score CTA: row-max exchange [tile parity][quadrant]
   B_XL = 35,                         // score CTA: row-sum exchange at a segment end
   B_PSTAGED = 36,                    // score CTA: P of a tile is in the staging buffer
@@ -129,19 +132,19 @@ enum : int {
   B_OFREE = 44,                      // value CTA: epilogue has read O
   B_DRAIN = 45,                      // both: final MMA drain
   B_QRFULL = 46,                     // score CTA: q^R of the segment has landed
-  B_QREMPTY = 47                     // score CTA: the segment's MMAs no longer read q^R
+  B_QREMPTY = 47,                    // score CTA: the segment's MMAs no longer read q^R
+  B_PLAN = 48                        // both: the split plan of this CTA's group is in PlanState
 };
 
 struct DecodeParams {
   const int32_t* seqlens;      // [B]
-  const int32_t* prefix;       // plan (splitkv.cuh)
-  const int32_t* gfirst;
-  const int32_t* segbase;
-  const int32_t* gstart;       // [G] first sequence of each group's run
+  int32_t* prefix;             // plan for the combine (splitkv.cuh), written by CTA 0: [B + 1]
+  int32_t* gfirst;             // [B]
+  int32_t* segbase;            // [B + 1]
   float2* ml;                  // [slots * n_rb, 128]        (m, l) per row
   uint4* opart;                // [slots * n_rb][64 column octets][128 rows] fp16 x 8: O / l per segment
   uint32_t* status;
-  const uint32_t* plan_ok;
+  uint32_t* plan_ok;           // written by CTA 0
   int B, S, H, Lmax, n_rb, G;
   float scale_log2;            // softmax_scale * log2(e)
   uint64_t timeout_ns;
@@ -154,38 +157,135 @@ struct TileInfo {
   bool dry;  // warm-up visit of a stand-in tile: compute only, no waits, no global reads or writes
 };
 
-// Tiles of group g in order (see splitkv.cuh for the plan), as a cursor.
+// The split plan as one CTA needs it (splitkv.cuh): the total tile count and
+// the state of the walk at the sequence holding the group's first tile.
+struct PlanState {
+  int64_t T;       // tiles of all sequences
+  int b0, x0, sb0;  // that sequence, its first flat tile, its first segment slot
+  int ok;          // every sequence length was valid
+};
+
+__device__ __forceinline__ int nseg_of(int64_t x0, int64_t x1, int64_t T, int G) {
+  return x1 > x0 ? group_of(x1 - 1, T, G) - group_of(x0, T, G) + 1 : 0;
+}
+
+// One warp builds the plan state of group g from the sequence lengths (two
+// passes over them); with write_global it also writes the plan arrays the
+// combine reads (the CTA holding group 0 does).
+__device__ void plan_scan(const DecodeParams& p, int g, bool write_global, PlanState* ps) {
+  const int lane = threadIdx.x & 31;
+  int64_t T = 0;
+  bool bad = false;
+  for (int base = 0; base < p.B; base += 256) {  // pass 1: total tiles, validity (8 loads in flight)
+    int L[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int b = base + u * 32 + lane;
+      L[u] = b < p.B ? p.seqlens[b] : p.S;
+    }
+    int t = 0;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      if (base + u * 32 + lane >= p.B) continue;
+      if (L[u] < p.S || L[u] > p.Lmax) bad = true;
+      else t += tiles_of(L[u]);
+    }
+    T += __reduce_add_sync(0xffffffffu, (unsigned)t);
+  }
+  bad = __any_sync(0xffffffffu, bad);
+  const int64_t beg = (bad || T == 0) ? 0 : (int64_t)g * T / p.G;
+  int64_t run_x = 0;
+  int run_sb = 0, b0 = 0, x0 = 0, sb0 = 0;
+  bool found = false;
+  for (int base = 0; base < p.B && !bad && (write_global || !found); base += 32) {  // pass 2
+    const int b = base + lane;
+    const int t = b < p.B ? tiles_of(p.seqlens[b]) : 0;
+    int it = t;  // inclusive scans over the warp
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, it, o);
+      if (lane >= o) it += y;
+    }
+    const int64_t x = run_x + it - t;  // first flat tile of sequence b
+    const int ns = nseg_of(x, x + t, T, p.G);
+    int is = ns;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, is, o);
+      if (lane >= o) is += y;
+    }
+    const int sb = run_sb + is - ns;  // its first segment slot
+    if (write_global && b < p.B) {
+      p.prefix[b] = (int32_t)x;
+      p.gfirst[b] = t > 0 ? group_of(x, T, p.G) : 0;
+      p.segbase[b] = sb;
+    }
+    const unsigned hit = __ballot_sync(0xffffffffu, t > 0 && x <= beg && beg < x + t);
+    if (!found && hit) {
+      const int src = __ffs(hit) - 1;
+      b0 = __shfl_sync(0xffffffffu, b, src);
+      x0 = __shfl_sync(0xffffffffu, (int)x, src);
+      sb0 = __shfl_sync(0xffffffffu, sb, src);
+      found = true;
+    }
+    run_x += __shfl_sync(0xffffffffu, it, 31);
+    run_sb += __shfl_sync(0xffffffffu, is, 31);
+  }
+  if (lane == 0) {
+    if (write_global) {
+      p.prefix[p.B] = (int32_t)T;
+      p.segbase[p.B] = run_sb;
+      *p.plan_ok = bad ? 0u : 1u;
+      if (bad) atomicOr(p.status, kDevErrBadSeqlen);
+    }
+    ps->T = T;
+    ps->b0 = b0;
+    ps->x0 = x0;
+    ps->sb0 = sb0;
+    ps->ok = (!bad && found) ? 1 : 0;
+  }
+}
+
+// Tiles of group g in order, as a cursor that follows the sequences from the
+// plan state on (prefix and segment slot carried along, lengths re-read).
 struct TileCursor {
-  int64_t beg, end;  // the group's flat tiles [beg, end)
-  int g, b, t, tb, te, i, k, slot, L;
+  int64_t beg, end, T;  // the group's flat tiles [beg, end) of T
+  int64_t x0;           // first flat tile of sequence b
+  int g, b, sb, t, tb, te, i, k, slot, L;
 };
 
 // Move c to the first sequence from c.b on that has tiles in the run.
 __device__ __forceinline__ bool cursor_seq(const DecodeParams& p, TileCursor& c) {
-  for (; c.b < p.B; ++c.b) {
-    const int64_t x0 = p.prefix[c.b], x1 = p.prefix[c.b + 1];
-    if (x0 >= c.end) return false;
-    if (x1 <= c.beg) continue;
-    c.tb = (int)(max(c.beg, x0) - x0);
-    c.te = (int)(min(c.end, x1) - x0);
-    c.t = c.tb;
-    c.slot = p.segbase[c.b] + (c.g - p.gfirst[c.b]);
-    c.L = p.seqlens[c.b];
-    return true;
+  while (c.b < p.B && c.x0 < c.end) {
+    const int L = p.seqlens[c.b];
+    const int64_t x1 = c.x0 + tiles_of(L);
+    if (x1 > c.beg) {
+      c.tb = (int)(max(c.beg, c.x0) - c.x0);
+      c.te = (int)(min(c.end, x1) - c.x0);
+      c.t = c.tb;
+      c.slot = c.sb + (c.g - group_of(c.x0, c.T, p.G));
+      c.L = L;
+      return true;
+    }
+    c.sb += nseg_of(c.x0, x1, c.T, p.G);
+    c.x0 = x1;
+    ++c.b;
   }
   return false;
 }
 
-__device__ __forceinline__ bool cursor_start(const DecodeParams& p, int g, TileCursor& c) {
-  const int64_t T = p.prefix[p.B];
-  if (T <= 0) return false;
-  c.beg = (int64_t)g * T / p.G;
-  c.end = (int64_t)(g + 1) * T / p.G;
+__device__ __forceinline__ bool cursor_start(const DecodeParams& p, int g, const PlanState& ps, TileCursor& c) {
+  if (!ps.ok || ps.T <= 0) return false;
+  c.T = ps.T;
+  c.beg = (int64_t)g * ps.T / p.G;
+  c.end = (int64_t)(g + 1) * ps.T / p.G;
   if (c.beg >= c.end) return false;
   c.g = g;
   c.i = 0;
   c.k = 0;
-  c.b = p.gstart[g];
+  c.b = ps.b0;
+  c.x0 = ps.x0;
+  c.sb = ps.sb0;
   return cursor_seq(p, c);
 }
 
@@ -193,6 +293,9 @@ __device__ __forceinline__ bool cursor_next(const DecodeParams& p, TileCursor& c
   ++c.i;
   if (++c.t < c.te) return true;
   ++c.k;
+  const int64_t x1 = c.x0 + tiles_of(c.L);
+  c.sb += nseg_of(c.x0, x1, c.T, p.G);
+  c.x0 = x1;
   ++c.b;
   return cursor_seq(p, c);
 }
@@ -202,11 +305,11 @@ __device__ __forceinline__ TileInfo cursor_tile(const TileCursor& c) {
                   false};
 }
 
-// Visit every tile of group g in order.
+// Visit every tile of group g in order (the plan state is in place).
 template <class F>
-__device__ __forceinline__ void for_each_tile(const DecodeParams& p, int g, F&& f) {
+__device__ __forceinline__ void for_each_tile(const DecodeParams& p, int g, const PlanState& ps, F&& f) {
   TileCursor c;
-  for (bool have = cursor_start(p, g, c); have; have = cursor_next(p, c))
+  for (bool have = cursor_start(p, g, ps, c); have; have = cursor_next(p, c))
     if (!f(cursor_tile(c))) return;
 }
 
@@ -215,21 +318,16 @@ __device__ __forceinline__ void for_each_tile(const DecodeParams& p, int g, F&& 
 // on have finished), then the dependency wait, then every tile of group g.
 // All visits go through the same call of f so that they run the same code.
 template <class F>
-__device__ __forceinline__ void for_each_tile_warm(const DecodeParams& p, int g, const volatile uint32_t* abort_flag,
-                                                   bool dry_first, F&& f) {
+__device__ __forceinline__ void for_each_tile_warm(const DecodeParams& p, int g, const PlanState& ps,
+                                                   uint64_t* plan_bar, const WaitCtx& wc, F&& f) {
   TileInfo ti{0, 0, kTok, 0, 0, 0, kTok, true, false, true};
   TileCursor c;
   bool have = true;
-  if (!dry_first) {
-    pdl_wait();  // q_cat and the plan come from the kernels before this one
-    have = *p.plan_ok != 0u && *abort_flag == 0u && cursor_start(p, g, c);
-    if (have) ti = cursor_tile(c);
-  }
   while (have) {
     if (!f(ti)) return;
     if (ti.dry) {
-      pdl_wait();
-      have = *p.plan_ok != 0u && *abort_flag == 0u && cursor_start(p, g, c);
+      pdl_wait();  // q_cat and the sequence lengths may come from the kernel before this one
+      have = mbar_wait(plan_bar, 0, wc) && *wc.abort_flag == 0u && cursor_start(p, g, ps, c);
     } else {
       have = cursor_next(p, c);
     }
@@ -290,7 +388,6 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       mbar_init(&bar[B_PVDONE + s], 1);
     }
     for (int s = 0; s < 8; ++s) mbar_init(&bar[B_XCH + s], 64);
-    mbar_init(&bar[B_QREADY], 256);
     mbar_init(&bar[B_XL], 256);
     mbar_init(&bar[B_PSTAGED], 256);
     mbar_init(&bar[B_PSFREE], 1);
@@ -298,6 +395,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     mbar_init(&bar[B_DRAIN], 1);
     mbar_init(&bar[B_QRFULL], 1);
     mbar_init(&bar[B_QREMPTY], 1);
+    mbar_init(&bar[B_PLAN], 1);
     if (rank == 1) {  // first phase of each P slot expects one slot's bytes
       mbar_arrive_expect_tx(&bar[B_PFULL + 0], kPTx);
       mbar_arrive_expect_tx(&bar[B_PFULL + 1], kPTx);
@@ -321,10 +419,20 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   tc_fence_after();
   cluster_sync();  // the peer's barriers exist before anyone arrives on them remotely
   pdl_trigger();
+  PlanState* plan = reinterpret_cast<PlanState*>(smem + kOffPlan);
   const bool rows = warp >= 4;
-  if (!rows) pdl_wait();  // q_cat and the plan come from the kernels before this one (row warps: later)
+  if (warp == 3) {
+    // The split plan, from the sequence lengths, which may come from the
+    // kernels before this one like q_cat (row warps: after their dry visit).
+    pdl_wait();
+    plan_scan(p, g, blockIdx.x == 0, plan);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bar[B_PLAN]);
+  } else if (!rows) {
+    pdl_wait();
+  }
   const uint32_t tmem = *tmem_slot;
-  const bool run = rows || ((*p.plan_ok != 0u) && (*abort_flag == 0u));
+  const bool run = rows || (warp < 3 && mbar_wait(&bar[B_PLAN], 0, wc) && plan->ok && *abort_flag == 0u);
 
   if (run && warp == 0) {
     // ------------------------------------------------ TMA producer (both CTAs)
@@ -341,7 +449,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         last_use[base + st] = pos;
         return st;
       };
-      for_each_tile(p, g, [&](const TileInfo& ti) {
+      for_each_tile(p, g, *plan, [&](const TileInfo& ti) {
         const int row0 = ti.b * p.Lmax + ti.t * kTok;
         if (rank == 0) {
           if (ti.first) {  // the segment's query rows: blocks 0..7 through the c ring, q^R to its buffer
@@ -387,12 +495,26 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     if (lane == 0) {
       if (rank == 0) {
         constexpr uint32_t idesc = idesc_bf16_f32(128, kTok, 0, 0);
-        for_each_tile(p, g, [&](const TileInfo& ti) {
+        for_each_tile(p, g, *plan, [&](const TileInfo& ti) {
           const int sb = ti.i & 1;                            // S buffer of this tile
           const uint32_t sph = (uint32_t)(ti.i >> 1) & 1u;    // its phase
-          if (ti.first) {  // q~ has been moved out of the c ring: release it; q^R must have landed
-            if (!mbar_wait(&bar[B_QREADY], (uint32_t)ti.k & 1u, wc)) return false;
-            for (int h = 0; h < 2; ++h) mbar_arrive(&bar[B_EMPTY + kBarC + cpos_q(ti.i, ti.k, h) % kCStages]);
+          if (ti.first) {
+            // q~ of the segment: its two c stages go into tensor memory by
+            // tcgen05.cp, after every MMA of the previous segment (which read
+            // the old q~) has completed; the copy is ordered before this
+            // thread's next MMAs.  q^R must have landed in its buffer.
+            if (ti.k > 0 && !mbar_wait(&bar[B_QREMPTY], (uint32_t)(ti.k - 1) & 1u, wc)) return false;
+            for (int h = 0; h < 2; ++h) {
+              const int q = cpos_q(ti.i, ti.k, h), st = q % kCStages;
+              if (!mbar_wait(&bar[B_FULL + kBarC + st], (uint32_t)(q / kCStages) & 1u, wc)) return false;
+              tc_fence_after();
+              const uint32_t sbase = smem_u32(smem + st * kCStage);
+#pragma unroll
+              for (int kk = 0; kk < 16; ++kk)  // 4 blocks x 4 slices of 16 columns
+                tmem_cp_128x256b(tmem + kQCol + (uint32_t)(h * 16 + kk) * 8,
+                                 smem_desc(sbase + (kk >> 2) * kBlk0 + (kk & 3) * 32, 16, 1024, 2));
+              mma_commit(&bar[B_EMPTY + kBarC + st]);  // the stage is free once the copy has read it
+            }
             if (!mbar_wait(&bar[B_QRFULL], (uint32_t)ti.k & 1u, wc)) return false;
           }
           if (!mbar_wait(&bar[B_SEMPTY + sb], sph ^ 1u, wc)) return false;
@@ -427,7 +549,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       } else {
         constexpr uint32_t idesc = idesc_bf16_f32(128, 256, 0, 1);
         int q = 0;
-        for_each_tile(p, g, [&](const TileInfo& ti) {
+        for_each_tile(p, g, *plan, [&](const TileInfo& ti) {
           const int slot = ti.i & 1;
           const uint32_t sph = (uint32_t)(ti.i >> 1) & 1u;
           if (!mbar_wait(&bar[B_PREADY + slot], sph, wc)) return false;
@@ -465,7 +587,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         // -------------------------------------------- score CTA: P copy into the value CTA
         const uint32_t p_remote = map_to_cta(smem_u32(smem + kOffP), 1);
         const uint32_t pfull_remote = map_to_cta(smem_u32(&bar[B_PFULL]), 1);
-        for_each_tile(p, g, [&](const TileInfo& ti) {
+        for_each_tile(p, g, *plan, [&](const TileInfo& ti) {
           const int slot = ti.i & 1;
           const uint32_t sph = (uint32_t)(ti.i >> 1) & 1u;
           if (!mbar_wait(&bar[B_PSTAGED], (uint32_t)ti.i & 1u, wc)) return false;
@@ -479,7 +601,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         });
       } else {
         // -------------------------------------------- value CTA: P-slot releaser
-        for_each_tile(p, g, [&](const TileInfo& ti) {
+        for_each_tile(p, g, *plan, [&](const TileInfo& ti) {
           const int slot = ti.i & 1;
           if (!mbar_wait(&bar[B_PVDONE + slot], (uint32_t)(ti.i >> 1) & 1u, wc)) return false;
           mbar_arrive_remote(&bar[B_PEMPTY + slot], 0);
@@ -504,32 +626,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       uint8_t* ps = smem + kOffPS;
       float m_ref = -INFINITY, l = 0.f;
       int limit = 0;
-      for_each_tile_warm(p, g, abort_flag, /*dry_first=*/hf == 1, [&](const TileInfo& ti) {
+      for_each_tile_warm(p, g, *plan, &bar[B_PLAN], wc, [&](const TileInfo& ti) {
         if (ti.first) {
           limit = valid ? ti.L - p.S + s_r + 1 : 0;
-          // q~ into tensor memory (block j at columns kQCol + 32 j); the
-          // blocks come through the c ring.  The group's first query rows are
-          // moved by the hf = 0 thread alone (its partner is in the dry visit
-          // then), later ones by both, four blocks each.
-          const bool whole = ti.i == 0;
-          if (!ti.dry && (!whole || hf == 0)) {
-            const int j0 = whole ? 0 : hf * 4, j1 = whole ? 8 : hf * 4 + 4;
-            for (int j = j0; j < j1; ++j) {
-              const int q = cpos_q(ti.i, ti.k, j >> 2), st = q % kCStages;
-              if (!warp_wait(&bar[B_FULL + kBarC + st], (uint32_t)(q / kCStages) & 1u, wc)) return false;
-              const uint8_t* rowp = smem + st * kCStage + (j & 3) * kBlk0 + r * 128;
-              uint32_t v[32];
-#pragma unroll
-              for (int ch = 0; ch < 8; ++ch) {  // logical chunk ch sits at ch ^ (r & 7)
-                const uint4 x = *reinterpret_cast<const uint4*>(rowp + ((ch ^ (r & 7)) << 4));
-                v[4 * ch] = x.x; v[4 * ch + 1] = x.y; v[4 * ch + 2] = x.z; v[4 * ch + 3] = x.w;
-              }
-              tmem_st32(tl + kQCol + (uint32_t)j * 32, v);
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive_n(&bar[B_QREADY], whole ? 2u : 1u);
-          }
           m_ref = -INFINITY;
           l = 0.f;
         }
@@ -580,7 +679,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         uint8_t* row = ps + hf * 16384 + r * 128;
         float lsum0 = 0.f, lsum1 = 0.f;
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {  // 2^(s * scale * log2 e - m) for 16 columns: two 16-byte chunks of P
+        for (int c = 0; c < 4; ++c) {  // 2^(s scale log2 e - m), 16 columns per pass
           uint32_t v[16];
           tmem_ld16(sc + (uint32_t)(c * 16), v);
           tmem_wait_ld();
@@ -627,7 +726,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       // ---------------------------------------- rescale, tail zeroing, epilogue
       const int wt = threadIdx.x - 128;  // 0..255
       int q = 0;  // running stage counter (as the producer's)
-      for_each_tile_warm(p, g, abort_flag, /*dry_first=*/true, [&](const TileInfo& ti) {
+      for_each_tile_warm(p, g, *plan, &bar[B_PLAN], wc, [&](const TileInfo& ti) {
         const int slot = ti.i & 1;
         const uint32_t sph = (uint32_t)(ti.i >> 1) & 1u;
         const int nsub = (ti.nvt + kSub - 1) / kSub;

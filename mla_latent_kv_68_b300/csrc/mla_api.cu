@@ -127,7 +127,7 @@ bool encode_decode_maps(DecodeMaps* m, const void* q_cat, const void* c_kv, cons
 // Workspace layout of mla_decode / mla_splitkv_combine.
 struct WsLayout {
   int n_rb = 0, G = 0, slots = 0;
-  size_t prefix = 0, gfirst = 0, segbase = 0, gstart = 0, ml = 0, opart = 0, total = 0;
+  size_t prefix = 0, gfirst = 0, segbase = 0, ml = 0, opart = 0, total = 0;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -142,7 +142,6 @@ WsLayout ws_layout(int B, int S, int H, int max_clusters) {
   w.prefix = off;  off = align256(off + sizeof(int32_t) * (B + 1));
   w.gfirst = off;  off = align256(off + sizeof(int32_t) * B);
   w.segbase = off; off = align256(off + sizeof(int32_t) * (B + 1));
-  w.gstart = off;  off = align256(off + sizeof(int32_t) * w.G);
   w.ml = off;      off = align256(off + sizeof(float) * 2 * (size_t)w.slots * w.n_rb * 128);
   w.opart = off;   off = align256(off + sizeof(uint16_t) * (size_t)w.slots * w.n_rb * 128 * 512);
   w.total = off;
@@ -387,34 +386,18 @@ mla_status mla_decode(const mla_bf16* q_cat, const mla_bf16* c_kv, const mla_bf1
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   cudaStream_t st = (cudaStream_t)stream;
 
-  mla::PlanParams pp;
-  pp.seqlens = seqlens;
-  pp.B = B;
-  pp.S = S;
-  pp.Lmax = Lmax;
-  pp.G = w.G;
-  pp.prefix = reinterpret_cast<int32_t*>(ws + w.prefix);
-  pp.gfirst = reinterpret_cast<int32_t*>(ws + w.gfirst);
-  pp.segbase = reinterpret_cast<int32_t*>(ws + w.segbase);
-  pp.gstart = reinterpret_cast<int32_t*>(ws + w.gstart);
-  pp.status = reinterpret_cast<uint32_t*>(ws);
-  pp.plan_ok = reinterpret_cast<uint32_t*>(ws) + 1;
-  const mla_status ps = launch_ex(mla::plan_kernel, dim3(1), dim3(1024), 0, st, true, 1, pp);
-  if (ps != MLA_OK) return ps;
-
   DecodeMaps maps;
   if (!encode_decode_maps(&maps, q_cat, c_kv, k_r, B, S, H, Lmax)) return MLA_ERR_INVALID_ARG;
 
   mla::DecodeParams p;
   p.seqlens = seqlens;
-  p.prefix = pp.prefix;
-  p.gfirst = pp.gfirst;
-  p.segbase = pp.segbase;
-  p.gstart = pp.gstart;
+  p.prefix = reinterpret_cast<int32_t*>(ws + w.prefix);
+  p.gfirst = reinterpret_cast<int32_t*>(ws + w.gfirst);
+  p.segbase = reinterpret_cast<int32_t*>(ws + w.segbase);
   p.ml = reinterpret_cast<float2*>(ws + w.ml);
   p.opart = reinterpret_cast<uint4*>(ws + w.opart);
-  p.status = pp.status;
-  p.plan_ok = pp.plan_ok;
+  p.status = reinterpret_cast<uint32_t*>(ws);
+  p.plan_ok = reinterpret_cast<uint32_t*>(ws) + 1;
   p.B = B;
   p.S = S;
   p.H = H;
@@ -563,34 +546,18 @@ extern "C" mla_status mla_decode_noalloc(const mla_bf16* q_cat, const mla_bf16* 
   if (!ws) return MLA_ERR_CUDA;
   cudaStream_t st = (cudaStream_t)stream;
   // Device errors go to the library status word; word [1] of the scratch is
-  // the plan's ok flag, rewritten by the plan kernel on every call.
+  // the plan's ok flag, rewritten by the decode kernel on every call.
   uint32_t* status = dev->kernel_status;
   uint32_t* plan_ok = reinterpret_cast<uint32_t*>(ws) + 1;
-
-  mla::PlanParams pp;
-  pp.seqlens = seqlens;
-  pp.B = B;
-  pp.S = S;
-  pp.Lmax = Lmax;
-  pp.G = w.G;
-  pp.prefix = reinterpret_cast<int32_t*>(ws + w.prefix);
-  pp.gfirst = reinterpret_cast<int32_t*>(ws + w.gfirst);
-  pp.segbase = reinterpret_cast<int32_t*>(ws + w.segbase);
-  pp.gstart = reinterpret_cast<int32_t*>(ws + w.gstart);
-  pp.status = status;
-  pp.plan_ok = plan_ok;
-  mla::plan_kernel<<<1, 1024, 0, st>>>(pp);
-  if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
 
   DecodeMaps maps;
   if (!encode_decode_maps(&maps, q_cat, c_kv, k_r, B, S, H, Lmax)) return MLA_ERR_INVALID_ARG;
 
   mla::DecodeParams p;
   p.seqlens = seqlens;
-  p.prefix = pp.prefix;
-  p.gfirst = pp.gfirst;
-  p.segbase = pp.segbase;
-  p.gstart = pp.gstart;
+  p.prefix = reinterpret_cast<int32_t*>(ws + w.prefix);
+  p.gfirst = reinterpret_cast<int32_t*>(ws + w.gfirst);
+  p.segbase = reinterpret_cast<int32_t*>(ws + w.segbase);
   p.ml = reinterpret_cast<float2*>(ws + w.ml);
   p.opart = reinterpret_cast<uint4*>(ws + w.opart);
   p.status = status;
@@ -621,9 +588,9 @@ extern "C" mla_status mla_decode_noalloc(const mla_bf16* q_cat, const mla_bf16* 
     return MLA_ERR_CUDA;
 
   mla::CombineParams cp;
-  cp.prefix = pp.prefix;
-  cp.gfirst = pp.gfirst;
-  cp.segbase = pp.segbase;
+  cp.prefix = p.prefix;
+  cp.gfirst = p.gfirst;
+  cp.segbase = p.segbase;
   cp.ml = p.ml;
   cp.opart = p.opart;
   cp.o_lat = reinterpret_cast<__nv_bfloat16*>(o_lat);

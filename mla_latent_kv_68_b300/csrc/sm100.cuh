@@ -271,6 +271,14 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
 }
 
 // Arrive once on `bar` when every MMA issued so far by this thread has completed.
+// Shared memory -> tensor memory copy of a 128-row x 32-byte slice described
+// by a matrix descriptor (the same form as an MMA operand's): row i lands in
+// lane i, eight consecutive 32-bit columns.  Asynchronous, issued by one
+// thread, and executed in order with that thread's MMAs.
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t s_desc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(s_desc) : "memory");
+}
+
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(

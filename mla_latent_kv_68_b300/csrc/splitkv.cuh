@@ -15,23 +15,14 @@
 // and cut into G equal runs, one per group of clusters.  Group g owns flat
 // tiles [floor(g T / G), floor((g+1) T / G)).  A sequence b contributes one
 // segment to every group its tiles touch; its segments get consecutive slot
-// numbers starting at segbase[b].
+// numbers starting at segbase[b].  The decode kernel works the plan out
+// itself from the sequence lengths (decode.cuh, plan_scan) and leaves the
+// arrays below (prefix, gfirst, segbase, plan_ok) for the combine.
 #pragma once
 
 #include "sm100.cuh"
 
 namespace mla {
-
-struct PlanParams {
-  const int32_t* seqlens;
-  int B, S, Lmax, G;
-  int32_t* prefix;   // [B+1] exclusive prefix of tiles per sequence; prefix[B] = T
-  int32_t* gfirst;   // [B] first group touching sequence b
-  int32_t* segbase;  // [B+1] exclusive prefix of segments per sequence
-  int32_t* gstart;   // [G] first sequence touched by each group
-  uint32_t* status;
-  uint32_t* plan_ok;
-};
 
 constexpr int kTileRows = 128;
 
@@ -40,97 +31,6 @@ __device__ __forceinline__ int tiles_of(int L) { return (L + kTileRows - 1) / kT
 // Group owning flat tile x: the largest g with floor(g T / G) <= x.
 __device__ __forceinline__ int group_of(int64_t x, int64_t T, int G) {
   return (int)(((x + 1) * G - 1) / T);
-}
-
-// Block-wide exclusive scan of one int per thread (blockDim.x a multiple of 32).
-__device__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  int inc = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int t = __shfl_up_sync(0xffffffffu, inc, o);
-    if (lane >= o) inc += t;
-  }
-  if (lane == 31) warp_sums[warp] = inc;
-  __syncthreads();
-  if (warp == 0) {
-    int w = lane < nw ? warp_sums[lane] : 0;
-    int winc = w;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int t = __shfl_up_sync(0xffffffffu, winc, o);
-      if (lane >= o) winc += t;
-    }
-    if (lane < nw) warp_sums[lane] = winc - w;
-    if (lane == nw - 1) warp_sums[32] = winc;
-  }
-  __syncthreads();
-  const int excl = warp_sums[warp] + inc - v;
-  *total = warp_sums[32];
-  __syncthreads();
-  return excl;
-}
-
-__global__ void __launch_bounds__(1024) plan_kernel(const PlanParams p) {
-  __shared__ int warp_sums[33];
-  __shared__ int bad;
-  pdl_trigger();
-  pdl_wait();  // the workspace may still be read by the previous step's kernels
-  const int nt = blockDim.x;
-  if (threadIdx.x == 0) bad = 0;
-  __syncthreads();
-  const int E = (p.B + nt - 1) / nt;
-  const int beg = min(p.B, (int)threadIdx.x * E), end = min(p.B, beg + E);
-
-  int local = 0;
-  for (int b = beg; b < end; ++b) {
-    const int L = p.seqlens[b];
-    if (L < p.S || L > p.Lmax) bad = 1;
-    else local += tiles_of(L);
-  }
-  int T;
-  int run = block_exclusive_scan(local, warp_sums, &T);
-  for (int b = beg; b < end; ++b) {
-    p.prefix[b] = run;
-    const int L = p.seqlens[b];
-    if (L >= p.S && L <= p.Lmax) run += tiles_of(L);
-  }
-  if (threadIdx.x == 0) p.prefix[p.B] = T;
-  __syncthreads();
-
-  local = 0;
-  for (int b = beg; b < end; ++b) {
-    const int x0 = p.prefix[b], x1 = p.prefix[b + 1];
-    int ns = 0, gf = 0;
-    if (x1 > x0) {
-      gf = group_of(x0, T, p.G);
-      ns = group_of(x1 - 1, T, p.G) - gf + 1;
-    }
-    p.gfirst[b] = gf;
-    local += ns;
-  }
-  int nseg_total;
-  run = block_exclusive_scan(local, warp_sums, &nseg_total);
-  for (int b = beg; b < end; ++b) {
-    p.segbase[b] = run;
-    const int x0 = p.prefix[b], x1 = p.prefix[b + 1];
-    if (x1 > x0) run += group_of(x1 - 1, T, p.G) - group_of(x0, T, p.G) + 1;
-  }
-  for (int g = threadIdx.x; g < p.G; g += nt) {  // largest b with prefix[b] <= floor(g T / G)
-    const int64_t tg = (int64_t)g * T / p.G;
-    int lo = 0, hi = p.B - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (p.prefix[mid] <= tg) lo = mid;
-      else hi = mid - 1;
-    }
-    p.gstart[g] = lo;
-  }
-  if (threadIdx.x == 0) {
-    p.segbase[p.B] = nseg_total;
-    *p.plan_ok = bad ? 0u : 1u;
-    if (bad) atomicOr(p.status, kDevErrBadSeqlen);
-  }
 }
 
 struct CombineParams {
