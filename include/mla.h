@@ -16,7 +16,8 @@
  * One decode step is five calls on one stream:
  *   mla_absorb_q -> mla_rope_apply (queries) -> mla_decode
  *   -> mla_splitkv_combine -> mla_up_project,
- * or four, with mla_absorb_rope_q doing the first two in one launch.
+ * or three: mla_absorb_rope_q (the first two in one launch) -> mla_decode
+ *   -> mla_combine_up_project (the last two, without storing o_lat).
  * The cache's k^R is rotated once, when it is written (mla_rope_apply on the
  * cache), because the pages cache the rotated key.
  *
@@ -200,6 +201,22 @@ mla_status mla_splitkv_combine(const void *workspace, size_t workspace_bytes, ml
  */
 mla_status mla_up_project(const mla_bf16 *o_lat, const mla_bf16 *W_UV, mla_bf16 *out, int B,
                           int S, int H, void *stream);
+
+/*
+ * mla_splitkv_combine followed by mla_up_project in one launch: the merged
+ * latent rows of each head go straight into the up-projection's operand in
+ * shared memory and o_lat is never stored.
+ *   o = W_UV[h] (sum_k w_k U_k / sum_k w_k),  w_k = l_k 2^(m_k - M)
+ * ("注意力计算": one softmax over all visible positions; "潜在向量的作用":
+ * o = W^UV o_lat).  `workspace` as left by mla_decode; W_UV [H,128,512]
+ * bf16; out [B,S,H,128] bf16.  B, S, H must match the mla_decode call.
+ * W_UV is read before the kernel waits for the one launched before it, so it
+ * must not be written by that kernel.  MLA_ERR_UNSUPPORTED if a sequence can
+ * be split into more than 96 segments on this device (more than 96
+ * co-resident decode clusters).
+ */
+mla_status mla_combine_up_project(const void *workspace, size_t workspace_bytes, const mla_bf16 *W_UV,
+                                  mla_bf16 *out, int B, int S, int H, void *stream);
 
 /*
  * Synchronise `stream`, return the device-side status recorded in

@@ -63,11 +63,12 @@ def lib():
         L.mla_decode.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, f32, vp, sz, vp]
         L.mla_splitkv_combine.argtypes = [vp, sz, vp, i32, i32, i32, vp]
         L.mla_up_project.argtypes = [vp, vp, vp, i32, i32, i32, vp]
+        L.mla_combine_up_project.argtypes = [vp, sz, vp, vp, i32, i32, i32, vp]
         L.mla_read_status.argtypes = [vp, vp]
         L.mla_decode_noalloc.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, f32, vp, vp]
         for n in ("mla_absorb_q", "mla_absorb_rope_q", "mla_absorb_rope_q_freq", "mla_rope_apply",
                   "mla_rope_apply_freq", "mla_rope_yarn_frequencies", "mla_decode",
-                  "mla_splitkv_combine", "mla_up_project", "mla_read_status",
+                  "mla_splitkv_combine", "mla_up_project", "mla_combine_up_project", "mla_read_status",
                   "mla_decode_noalloc"):
             getattr(L, n).restype = i32
         _lib = L
@@ -237,6 +238,17 @@ def up_project(o_lat, W_UV, out, stream=None):
            "mla_up_project")
 
 
+def combine_up_project(workspace, W_UV, out, stream=None):
+    """mla_splitkv_combine + mla_up_project in one launch: the merged latent
+    rows go straight into the up-projection, o_lat is not stored."""
+    B, S, H, _ = out.shape
+    _need(out, "out", shape=(B, S, H, D_V))
+    _need(W_UV, "W_UV", shape=(H, D_V, D_C))
+    _need(workspace, "workspace", dtype=torch.uint8)
+    _check(lib().mla_combine_up_project(_ptr(workspace), workspace.numel(), _ptr(W_UV), _ptr(out), B, S, H,
+                                        _stream(stream)), "mla_combine_up_project")
+
+
 def decode_noalloc(q_cat, c_kv, k_r, seqlens, o_lat, softmax_scale=SOFTMAX_SCALE, stream=None):
     """mla_decode + mla_splitkv_combine with the library's own fixed scratch
     array instead of a caller workspace, for callers that cannot allocate
@@ -295,6 +307,9 @@ class DecodeStep:
         decode(self.q_cat, c_kv, k_r, seqlens, self.workspace, scale, stream)
 
     def project(self, W_UV, stream=None):
+        # two launches: measured faster inside the pipelined step than the
+        # fused combine_up_project (the small combine CTAs start beside the
+        # decode's last clusters)
         splitkv_combine(self.workspace, self.o_lat, stream)
         up_project(self.o_lat, W_UV, self.out, stream)
 

@@ -13,6 +13,7 @@
 #include "mla.h"
 
 #include "absorb.cuh"
+#include "combine_up.cuh"
 #include "decode.cuh"
 #include "rope.cuh"
 #include "splitkv.cuh"
@@ -64,7 +65,9 @@ const DeviceInfo* device_info() {
       cudaFuncSetAttribute(mla::absorb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)mla::absorb_smem_bytes(256)) != cudaSuccess ||
       cudaFuncSetAttribute(mla::up_project_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)mla::up_smem_bytes(64)) != cudaSuccess)
+                           (int)mla::up_smem_bytes(64)) != cudaSuccess ||
+      cudaFuncSetAttribute(mla::combine_up_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)mla::cu_smem_bytes(mla::kCUTile)) != cudaSuccess)
     return nullptr;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -473,6 +476,50 @@ mla_status mla_up_project(const mla_bf16* o_lat, const mla_bf16* W_UV, mla_bf16*
   const dim3 grid(H, (unsigned)((BS + n_tile - 1) / n_tile));
   return launch_ex(mla::up_project_kernel, grid, dim3(mla::kUpThreads), mla::up_smem_bytes(n_tile),
                    (cudaStream_t)stream, true, 1, tw, to, p);
+}
+
+mla_status mla_combine_up_project(const void* workspace, size_t workspace_bytes, const mla_bf16* W_UV,
+                                  mla_bf16* out, int B, int S, int H, void* stream) {
+  if (!W_UV || !out || !aligned16(W_UV) || !aligned16(out)) return MLA_ERR_INVALID_ARG;
+  if (B < 1 || S < 1 || H < 1) return MLA_ERR_INVALID_ARG;
+  if (!decode_shape_ok(B, S, H)) return MLA_ERR_UNSUPPORTED;
+  const long long BS = (long long)B * S;
+  if (BS > 65535LL * mla::kCUTile) return MLA_ERR_UNSUPPORTED;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return MLA_ERR_WORKSPACE;
+  const DeviceInfo* dev = device_info();
+  if (!dev) return MLA_ERR_CUDA;
+  const WsLayout w = ws_layout(B, S, H, dev->max_clusters);
+  if (workspace_bytes < w.total) return MLA_ERR_WORKSPACE;
+  if (w.G > 32 * mla::kCUSegLanes) return MLA_ERR_UNSUPPORTED;  // more segments per row than lanes hold
+  const uint8_t* ws = static_cast<const uint8_t*>(workspace);
+  const int n_tile = BS >= mla::kCUTile ? mla::kCUTile : (int)((BS + 15) / 16 * 16);
+  CUtensorMap tw;
+  // W_UV [H*128 v-rows][512 k] seen as [64 k][H*128 rows][8 k-blocks]: one box = 2 atoms
+  const cuuint64_t wd[3] = {64, (cuuint64_t)H * 128, 8};
+  const cuuint64_t wst[2] = {1024, 128};
+  const cuuint32_t wb[3] = {64, 128, 2};
+  if (!encode_tiled(&tw, W_UV, 3, wd, wst, wb)) return MLA_ERR_INVALID_ARG;
+  mla::CombineUpParams p;
+  p.prefix = reinterpret_cast<const int32_t*>(ws + w.prefix);
+  p.gfirst = reinterpret_cast<const int32_t*>(ws + w.gfirst);
+  p.segbase = reinterpret_cast<const int32_t*>(ws + w.segbase);
+  p.ml = reinterpret_cast<const float2*>(ws + w.ml);
+  p.opart = reinterpret_cast<const uint4*>(ws + w.opart);
+  p.plan_ok = reinterpret_cast<const uint32_t*>(ws) + 1;
+  p.out = reinterpret_cast<__nv_bfloat16*>(out);
+  p.B = B;
+  p.S = S;
+  p.H = H;
+  p.n_rb = w.n_rb;
+  p.G = w.G;
+  p.BS = (int)BS;
+  p.n_tile = n_tile;
+  p.tmem_cols = pow2_at_least((uint32_t)n_tile);
+  p.status = reinterpret_cast<uint32_t*>(const_cast<uint8_t*>(ws));
+  p.timeout_ns = kTimeoutNs;
+  const dim3 grid(H, (unsigned)((BS + n_tile - 1) / n_tile));
+  return launch_ex(mla::combine_up_kernel, grid, dim3(mla::kCUTile * 32), mla::cu_smem_bytes(n_tile),
+                   (cudaStream_t)stream, true, 1, tw, p);
 }
 
 mla_status mla_read_status(void* workspace, void* stream) {

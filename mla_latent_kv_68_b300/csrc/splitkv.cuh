@@ -55,9 +55,12 @@ __device__ __forceinline__ bool group_empty(int g, int64_t T, int G) {
 // Block = one 128-row block of one sequence and kCombineCols latent columns;
 // thread = one query row.  Partials are stored as column octets x rows of
 // 8 fp16, so every 16-byte load of a warp reads 512 consecutive bytes.  The
-// (m, l) of all segments are read first; the partial columns of two segments
-// are then loaded together so that the few L2 round trips of a row overlap.
+// loads of a thread do not depend on one another: the (m, l) and the columns
+// of up to kSegBatch segments are requested together, so a row block with
+// that many segments costs one memory round trip, and longer ones fold batch
+// after batch into running sums kept relative to the largest m so far.
 constexpr int kCombineCols = 32;
+constexpr int kSegBatch = 4;
 
 __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
   pdl_trigger();
@@ -70,51 +73,50 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
   if (*p.plan_ok == 0u) return;
   const int k0 = p.segbase[b], k1 = p.segbase[b + 1], g0 = p.gfirst[b];
   const int64_t T = p.prefix[p.B];
+  const bool may_be_empty = T < p.G;  // only then can a group own no tile
 
-  float M = -INFINITY;
-  for (int k = k0; k < k1; ++k) {
-    if (group_empty(g0 + k - k0, T, p.G)) continue;
-    const float2 v = p.ml[((size_t)k * p.n_rb + rb) * 128 + r];
-    if (v.y > 0.f) M = fmaxf(M, v.x);
-  }
+  float M = -INFINITY, den = 0.f;
   float acc[kCombineCols];
 #pragma unroll
   for (int i = 0; i < kCombineCols; ++i) acc[i] = 0.f;
-  float den = 0.f;
-  for (int k = k0; k < k1; k += 2) {
-    float w[2];
-    const uint4* src[2];
+  for (int kb = k0; kb < k1; kb += kSegBatch) {
+    float2 ml[kSegBatch];
+    uint4 x[kSegBatch][kCombineCols / 8];
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const int kk = k + u;
-      w[u] = 0.f;
-      src[u] = p.opart;
-      if (kk < k1 && !group_empty(g0 + kk - k0, T, p.G)) {
-        const size_t idx = (size_t)kk * p.n_rb + rb;
-        const float2 v = p.ml[idx * 128 + r];
-        if (v.y > 0.f) {
-          w[u] = exp2f(v.x - M) * v.y;
-          den += w[u];
-          src[u] = p.opart + (idx * 64 + c0 / 8) * 128 + r;
-        }
-      }
-    }
-    uint4 x[2][kCombineCols / 8];
-#pragma unroll
-    for (int u = 0; u < 2; ++u)
+    for (int u = 0; u < kSegBatch; ++u) {
+      const int k = kb + u;
+      const bool ok = k < k1 && !(may_be_empty && group_empty(g0 + k - k0, T, p.G));
+      const size_t idx = (size_t)k * p.n_rb + rb;
+      ml[u] = ok ? __ldg(&p.ml[idx * 128 + r]) : make_float2(0.f, 0.f);
 #pragma unroll
       for (int c = 0; c < kCombineCols / 8; ++c)
-        x[u][c] = w[u] != 0.f ? __ldg(src[u] + (size_t)c * 128) : make_uint4(0u, 0u, 0u, 0u);
+        x[u][c] = ok ? __ldg(p.opart + (idx * 64 + c0 / 8 + c) * 128 + r) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    float Mb = M;
 #pragma unroll
-    for (int c = 0; c < kCombineCols / 8; ++c) {
-      const uint32_t* a = reinterpret_cast<const uint32_t*>(&x[0][c]);
-      const uint32_t* b = reinterpret_cast<const uint32_t*>(&x[1][c]);
+    for (int u = 0; u < kSegBatch; ++u)
+      if (ml[u].y > 0.f) Mb = fmaxf(Mb, ml[u].x);
+    if (Mb > M) {  // the m are integers: exact powers of two
+      const float sc = M == -INFINITY ? 0.f : exp2f(M - Mb);
+      den *= sc;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 fa = __half22float2(*reinterpret_cast<const __half2*>(&a[e]));
-        const float2 fb = __half22float2(*reinterpret_cast<const __half2*>(&b[e]));
-        acc[8 * c + 2 * e] += w[0] * fa.x + w[1] * fb.x;
-        acc[8 * c + 2 * e + 1] += w[0] * fa.y + w[1] * fb.y;
+      for (int i = 0; i < kCombineCols; ++i) acc[i] *= sc;
+      M = Mb;
+    }
+#pragma unroll
+    for (int u = 0; u < kSegBatch; ++u) {
+      if (!(ml[u].y > 0.f)) continue;  // no segment, or no visible row in it
+      const float w = exp2f(ml[u].x - M) * ml[u].y;
+      den += w;
+#pragma unroll
+      for (int c = 0; c < kCombineCols / 8; ++c) {
+        const uint32_t* h = reinterpret_cast<const uint32_t*>(&x[u][c]);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h[e]));
+          acc[8 * c + 2 * e] += w * f.x;
+          acc[8 * c + 2 * e + 1] += w * f.y;
+        }
       }
     }
   }
