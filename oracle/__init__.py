@@ -13,6 +13,7 @@ from .oracle import (  # noqa: F401
     rope_theta,
     yarn_theta,
     decode,
+    cache_append,
     absorb,
     up_project,
     latent_attention,

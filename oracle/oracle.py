@@ -167,6 +167,25 @@ def decode(q_nope, q_rope, c_kv, k_r, W_UK, W_UV, seqlens, *, softmax_scale=None
     return (out, wsum) if return_wsum else out
 
 
+def cache_append(h, W_DKV, W_KR, pos, *, rope_base: float = 10000.0, theta=None):
+    """The cache entry of new tokens ("DeepSeek-V3" (ekkoxiao.github.io),
+    "Multi-Head Latent Attention / KeyValue"):
+        c_t^KV = W^DKV h_t,        k_t^R = RoPE_t(W^KR h_t),
+    h [N, d], W_DKV [d_c, d], W_KR [d_r, d], pos [N] (the position t of each
+    token).  Returns (c [N, d_c], k_r [N, d_r]) in fp64.  The down-projections
+    are plain matrix products (numpy, fp64); the rotation is this oracle's
+    RoPE (base 10000, or explicit frequencies theta)."""
+    hh = np.asarray(h, np.float64)
+    wd = np.asarray(W_DKV, np.float64)
+    wr = np.asarray(W_KR, np.float64)
+    N, d = hh.shape
+    assert wd.shape[1] == d and wr.shape[1] == d
+    c = hh @ wd.T
+    k_pre = hh @ wr.T
+    k_r = rope(k_pre, pos, rope_base) if theta is None else rope_theta(k_pre, pos, theta)
+    return c, k_r
+
+
 def absorb(q_nope, W_UK):
     """q~[n,h,:] = W_UK[h]^T q_nope[n,h,:].  q_nope [N,H,d_h], W_UK [H,d_h,d_c]."""
     qn, code = _arr(q_nope)
