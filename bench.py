@@ -204,6 +204,41 @@ def _config(args, x):
                      if getattr(args, "rope", "plain") == "yarn" else "plain (base 10000)")}
 
 
+APPEND_D = 7168  # hidden size of the appended tokens (the pages leave d unstated)
+
+
+def _time_append(args, x, d, dev, stream, flush_l2, theta, mb):
+    """The cache-append step (next to the decode step, not part of its time):
+    the step's B*S new tokens, c = W^DKV h and k^R = RoPE(W^KR h) written at
+    their positions, recorded in a graph and replayed after an L2 flush."""
+    B, S = x["B"], x["S"]
+    g = torch.Generator().manual_seed(68100)
+    h = torch.randn(B, S, APPEND_D, generator=g).to(torch.bfloat16).to(dev)
+    wd = (torch.randn(512, APPEND_D, generator=g) / APPEND_D ** 0.5).to(torch.bfloat16).to(dev)
+    wr = (torch.randn(64, APPEND_D, generator=g) / APPEND_D ** 0.5).to(torch.bfloat16).to(dev)
+    ws = mb.cache_append_workspace(B, S, APPEND_D, device=dev)
+    call = (h, wd, wr, d["seqlens"], d["c_kv"], d["k_r"], ws)
+    for _ in range(max(3, args.warmup)):
+        mb.cache_append(*call, theta=theta)
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr):
+        mb.cache_append(*call, theta=theta)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    torch.cuda.synchronize(dev)
+    for e in ev:
+        flush_l2()
+        e[0].record(stream)
+        gr.replay()
+        e[1].record(stream)
+    torch.cuda.synchronize(dev)
+    if mb.read_status(ws) != mb.MLA_OK:
+        raise RuntimeError("device status not clean after the cache-append steps")
+    us = statistics.mean(e[0].elapsed_time(e[1]) for e in ev) * 1000
+    nbytes = (512 + 64) * APPEND_D * 2 + B * S * APPEND_D * 2 + B * S * (512 + 64) * 2
+    return {"workload": f"B={B} S={S} new tokens, d={APPEND_D}", "us": round(us, 3), "bytes": nbytes,
+            "launches": 2}
+
+
 def run_ours(args, x, rank, world, local_rank):
     from mla_latent_kv_68_b300 import binding as mb
 
@@ -291,6 +326,8 @@ def run_ours(args, x, rank, world, local_rank):
     ev_eager = timed(lambda e: e2e_body(e, replay=False), 2)
     eager_us = _max_over_ranks(statistics.mean(e[0].elapsed_time(e[1]) for e in ev_eager) * 1000, world)
 
+    app = _time_append(args, x, d, dev, stream, flush_l2, theta, mb)
+
     if rank != 0:
         return
     hbm, tf_burst, tf_sust, src = _peaks()
@@ -318,6 +355,8 @@ def run_ours(args, x, rank, world, local_rank):
         "e2e": {"value": round(e2e_us, 3), "unit": "us/step", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "path": "pinned host -> H2D -> step graph -> D2H",
                 "eager_calls_value": round(eager_us, 3)},
+        "append": {**app, "achieved_gbs": round(app["bytes"] / (app["us"] * 1e-6) / 1e9, 1),
+                   "frac": round(app["bytes"] / (app["us"] * 1e-6) / 1e9 / hbm, 4)},
         "gpu_launches": mb.DecodeStep.LAUNCHES_PER_STEP * args.steps,
         "clocks": clocks.summary(),
     }

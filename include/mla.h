@@ -219,6 +219,37 @@ mla_status mla_combine_up_project(const void *workspace, size_t workspace_bytes,
                                   mla_bf16 *out, int B, int S, int H, void *stream);
 
 /*
+ * Bytes of device workspace mla_cache_append needs (fp32 partial products of
+ * the down-projection and a status word); 0 if the shape is unsupported.
+ */
+size_t mla_cache_append_workspace_size(int B, int S, int d);
+
+/*
+ * The cache entries of the step's new tokens ("KeyValue"):
+ *   c_t^KV = W^DKV h_t,   k_t^R = RoPE_t(W^KR h_t),
+ * fp32 accumulation on the tensor cores, the RoPE angle reduced in fp64, both
+ * rounded to bf16 and written at the tokens' positions
+ * t = seqlens[b] - S + s (so seqlens already counts the new tokens, as
+ * mla_decode expects):
+ *   h      [B,S,d]   bf16 hidden states of the new tokens, d a multiple of 64
+ *   W_DKV  [512,d]   bf16,   W_KR [64,d] bf16
+ *   c_kv   [B,Lmax,512] bf16, k_r [B,Lmax,64] bf16: rows t are written, no
+ *          other row is touched
+ *   theta  host [32] RoPE frequencies (mla_rope_yarn_frequencies), or NULL
+ *          for theta_j = 10000^(-2j/64)
+ *   workspace >= mla_cache_append_workspace_size(B, S, d) bytes, 256-byte
+ *          aligned; its first word is a status word (mla_read_status): a
+ *          position outside [0, Lmax) sets MLA_ERR_BAD_SEQLEN and skips the
+ *          token.
+ * The weights are read before the kernel waits for the one launched before
+ * it on the stream, so they must not be written by that kernel.
+ */
+mla_status mla_cache_append(const mla_bf16 *h, const mla_bf16 *W_DKV, const mla_bf16 *W_KR,
+                            const int32_t *seqlens, mla_bf16 *c_kv, mla_bf16 *k_r, int B, int S, int d,
+                            int Lmax, const double *theta, void *workspace, size_t workspace_bytes,
+                            void *stream);
+
+/*
  * Synchronise `stream`, return the device-side status recorded in
  * `workspace` by earlier mla_decode calls (MLA_OK, MLA_ERR_BAD_SEQLEN or
  * MLA_ERR_TIMEOUT; MLA_ERR_CUDA if the stream reports an error) and clear it.

@@ -19,6 +19,8 @@ LIB_PATH = os.path.join(_PKG, "libmla.so")
 HEADER_PATH = os.path.join(os.path.dirname(_PKG), "include", "mla.h")
 
 MLA_OK = 0
+MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED, MLA_ERR_WORKSPACE, MLA_ERR_CUDA = 1, 2, 3, 4
+MLA_ERR_BAD_SEQLEN, MLA_ERR_TIMEOUT = 5, 6
 STATUS_NAMES = {0: "MLA_OK", 1: "MLA_ERR_INVALID_ARG", 2: "MLA_ERR_UNSUPPORTED",
                 3: "MLA_ERR_WORKSPACE", 4: "MLA_ERR_CUDA", 5: "MLA_ERR_BAD_SEQLEN",
                 6: "MLA_ERR_TIMEOUT"}
@@ -64,11 +66,15 @@ def lib():
         L.mla_splitkv_combine.argtypes = [vp, sz, vp, i32, i32, i32, vp]
         L.mla_up_project.argtypes = [vp, vp, vp, i32, i32, i32, vp]
         L.mla_combine_up_project.argtypes = [vp, sz, vp, vp, i32, i32, i32, vp]
+        L.mla_cache_append_workspace_size.restype = sz
+        L.mla_cache_append_workspace_size.argtypes = [i32, i32, i32]
+        L.mla_cache_append.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, sz, vp]
         L.mla_read_status.argtypes = [vp, vp]
         L.mla_decode_noalloc.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, f32, vp, vp]
         for n in ("mla_absorb_q", "mla_absorb_rope_q", "mla_absorb_rope_q_freq", "mla_rope_apply",
                   "mla_rope_apply_freq", "mla_rope_yarn_frequencies", "mla_decode",
                   "mla_splitkv_combine", "mla_up_project", "mla_combine_up_project", "mla_read_status",
+                  "mla_cache_append",
                   "mla_decode_noalloc"):
             getattr(L, n).restype = i32
         _lib = L
@@ -206,6 +212,32 @@ def decode_workspace_size(B: int, S: int, H: int) -> int:
 def new_workspace(B: int, S: int, H: int, device=None) -> torch.Tensor:
     """Zero-filled byte workspace for mla_decode / mla_splitkv_combine."""
     return torch.zeros(decode_workspace_size(B, S, H), dtype=torch.uint8, device=device or "cuda")
+
+
+def cache_append_workspace(B: int, S: int, d: int, device=None) -> torch.Tensor:
+    """Zero-filled byte workspace for mla_cache_append."""
+    n = lib().mla_cache_append_workspace_size(B, S, d)
+    if n == 0:
+        raise ValueError(f"unsupported cache-append shape B={B} S={S} d={d}")
+    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def cache_append(h, W_DKV, W_KR, seqlens, c_kv, k_r, workspace, theta=None, stream=None):
+    """c_kv[b, t] = W_DKV h[b, s] and k_r[b, t] = RoPE_t(W_KR h[b, s]) at
+    t = seqlens[b] - S + s (frequencies base 10000, or the 32 in `theta`)."""
+    B, S, d = h.shape
+    Lmax = c_kv.shape[1]
+    _need(h, "h", shape=(B, S, d))
+    _need(W_DKV, "W_DKV", shape=(D_C, d))
+    _need(W_KR, "W_KR", shape=(D_R, d))
+    _need(seqlens, "seqlens", dtype=torch.int32, shape=(B,))
+    _need(c_kv, "c_kv", shape=(B, Lmax, D_C))
+    _need(k_r, "k_r", shape=(B, Lmax, D_R))
+    _need(workspace, "workspace", dtype=torch.uint8)
+    th = None if theta is None else _theta_arg(theta)
+    _check(lib().mla_cache_append(_ptr(h), _ptr(W_DKV), _ptr(W_KR), _ptr(seqlens), _ptr(c_kv), _ptr(k_r),
+                                  B, S, d, Lmax, th, _ptr(workspace), workspace.numel(), _stream(stream)),
+           "mla_cache_append")
 
 
 def decode(q_cat, c_kv, k_r, seqlens, workspace, softmax_scale=SOFTMAX_SCALE, stream=None):

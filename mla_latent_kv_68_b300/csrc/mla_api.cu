@@ -13,6 +13,7 @@
 #include "mla.h"
 
 #include "absorb.cuh"
+#include "append.cuh"
 #include "combine_up.cuh"
 #include "decode.cuh"
 #include "rope.cuh"
@@ -67,7 +68,9 @@ const DeviceInfo* device_info() {
       cudaFuncSetAttribute(mla::up_project_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)mla::up_smem_bytes(64)) != cudaSuccess ||
       cudaFuncSetAttribute(mla::combine_up_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)mla::cu_smem_bytes(mla::kCUTile)) != cudaSuccess)
+                           (int)mla::cu_smem_bytes(mla::kCUTile)) != cudaSuccess ||
+      cudaFuncSetAttribute(mla::append_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)mla::app_smem_bytes(256)) != cudaSuccess)
     return nullptr;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -520,6 +523,69 @@ mla_status mla_combine_up_project(const void* workspace, size_t workspace_bytes,
   const dim3 grid(H, (unsigned)((BS + n_tile - 1) / n_tile));
   return launch_ex(mla::combine_up_kernel, grid, dim3(mla::kCUTile * 32), mla::cu_smem_bytes(n_tile),
                    (cudaStream_t)stream, true, 1, tw, p);
+}
+
+size_t mla_cache_append_workspace_size(int B, int S, int d) {
+  if (B < 1 || S < 1 || d < 64 || (d & 63) != 0) return 0;
+  const size_t ks = (size_t)(d + mla::kAppKc - 1) / mla::kAppKc;
+  return 256 + align256(sizeof(float) * ks * (size_t)B * S * mla::kAppCols);
+}
+
+mla_status mla_cache_append(const mla_bf16* h, const mla_bf16* W_DKV, const mla_bf16* W_KR,
+                            const int32_t* seqlens, mla_bf16* c_kv, mla_bf16* k_r, int B, int S, int d,
+                            int Lmax, const double* theta, void* workspace, size_t workspace_bytes,
+                            void* stream) {
+  if (!h || !W_DKV || !W_KR || !seqlens || !c_kv || !k_r || !aligned16(h) || !aligned16(W_DKV) ||
+      !aligned16(W_KR) || !aligned16(c_kv) || !aligned16(k_r))
+    return MLA_ERR_INVALID_ARG;
+  if (B < 1 || S < 1 || Lmax < S || d < 64) return MLA_ERR_INVALID_ARG;
+  if ((d & 63) != 0 || d > (1 << 20)) return MLA_ERR_UNSUPPORTED;
+  const long long BS = (long long)B * S;
+  if (BS > 65535LL * 256 || (long long)B * Lmax > 0x7fffffffLL) return MLA_ERR_UNSUPPORTED;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return MLA_ERR_WORKSPACE;
+  if (workspace_bytes < mla_cache_append_workspace_size(B, S, d)) return MLA_ERR_WORKSPACE;
+  mla::RopeTheta th = base_theta(10000.0);
+  if (theta && !copy_theta(theta, &th)) return MLA_ERR_INVALID_ARG;
+  const DeviceInfo* dev = device_info();
+  if (!dev) return MLA_ERR_CUDA;
+  const int ks = (d + mla::kAppKc - 1) / mla::kAppKc;
+  const int n_tile = BS >= 256 ? 256 : (int)((BS + 15) / 16 * 16);
+  // row-major [rows][d] seen as [64 columns][rows][d / 64 atoms]: one box = four
+  // 128-byte-swizzle atoms of 128 (weights) or n_tile (tokens) rows
+  const cuuint64_t nat = (cuuint64_t)(d / 64);
+  const cuuint64_t str[2] = {(cuuint64_t)d * 2, 128};
+  const cuuint64_t dd[3] = {64, 512, nat}, dr[3] = {64, 64, nat}, dh[3] = {64, (cuuint64_t)BS, nat};
+  const cuuint32_t bw[3] = {64, 128, 4}, bh[3] = {64, (cuuint32_t)n_tile, 4};
+  CUtensorMap twd, twr, th_map;
+  if (!encode_tiled(&twd, W_DKV, 3, dd, str, bw) || !encode_tiled(&twr, W_KR, 3, dr, str, bw) ||
+      !encode_tiled(&th_map, h, 3, dh, str, bh))
+    return MLA_ERR_INVALID_ARG;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  mla::AppendParams p;
+  p.part = reinterpret_cast<float*>(ws + 256);
+  p.BS = (int)BS;
+  p.n_tile = n_tile;
+  p.ks = ks;
+  p.tmem_cols = pow2_at_least((uint32_t)n_tile);
+  p.status = reinterpret_cast<uint32_t*>(ws);
+  p.timeout_ns = kTimeoutNs;
+  cudaStream_t st = (cudaStream_t)stream;
+  const dim3 grid(5, (unsigned)ks, (unsigned)((BS + n_tile - 1) / n_tile));
+  const mla_status s1 = launch_ex(mla::append_gemm_kernel, grid, dim3(mla::kAppThreads),
+                                  mla::app_smem_bytes(n_tile), st, true, 1, twd, twr, th_map, p);
+  if (s1 != MLA_OK) return s1;
+  mla::AppendFinalizeParams f;
+  f.part = p.part;
+  f.seqlens = seqlens;
+  f.c_kv = reinterpret_cast<__nv_bfloat16*>(c_kv);
+  f.k_r = reinterpret_cast<__nv_bfloat16*>(k_r);
+  f.status = p.status;
+  f.BS = (int)BS;
+  f.S = S;
+  f.ks = ks;
+  f.Lmax = Lmax;
+  return launch_ex(mla::append_finalize_kernel, dim3((unsigned)BS), dim3(mla::kAppCols / 2), 0, st, true, 1,
+                   f, th);
 }
 
 mla_status mla_read_status(void* workspace, void* stream) {

@@ -81,6 +81,15 @@ def _ptr(a):
     return ctypes.c_void_p(a.ctypes.data)
 
 
+def _f64(x):
+    """Inputs as fp64: uint16 arrays are raw bf16 bits (widened exactly), as
+    for every other entry of this oracle."""
+    a, code = _arr(x)
+    if code == BF16:
+        return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return a
+
+
 def _check(rc, what):
     if rc != 0:
         raise ValueError(f"oracle {what} failed with code {rc}")
@@ -171,13 +180,11 @@ def cache_append(h, W_DKV, W_KR, pos, *, rope_base: float = 10000.0, theta=None)
     """The cache entry of new tokens ("DeepSeek-V3" (ekkoxiao.github.io),
     "Multi-Head Latent Attention / KeyValue"):
         c_t^KV = W^DKV h_t,        k_t^R = RoPE_t(W^KR h_t),
-    h [N, d], W_DKV [d_c, d], W_KR [d_r, d], pos [N] (the position t of each
-    token).  Returns (c [N, d_c], k_r [N, d_r]) in fp64.  The down-projections
+    h [N, d], W_DKV [d_c, d], W_KR [d_r, d] (fp64, or uint16 bf16 bits),
+    pos [N] (the position t of each token).  Returns (c [N, d_c], k_r [N, d_r]) in fp64.  The down-projections
     are plain matrix products (numpy, fp64); the rotation is this oracle's
     RoPE (base 10000, or explicit frequencies theta)."""
-    hh = np.asarray(h, np.float64)
-    wd = np.asarray(W_DKV, np.float64)
-    wr = np.asarray(W_KR, np.float64)
+    hh, wd, wr = _f64(h), _f64(W_DKV), _f64(W_KR)
     N, d = hh.shape
     assert wd.shape[1] == d and wr.shape[1] == d
     c = hh @ wd.T

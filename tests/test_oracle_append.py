@@ -81,3 +81,16 @@ def test_yarn_frequencies_change_only_the_key():
     np.testing.assert_array_equal(c0, c1)
     np.testing.assert_allclose(k1, oracle.rope_theta(h @ wr.T, pos, th), rtol=0, atol=1e-12)
     assert not np.allclose(k0, k1)
+
+
+def test_bf16_bit_inputs_read_as_their_values():
+    wd, wr, rng = _w(6)
+    h = rng.standard_normal((2, D))
+    to_bits = lambda a: (np.asarray(a, np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    from_bits = lambda b: (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    hb, wdb, wrb = to_bits(h), to_bits(wd), to_bits(wr)   # truncated to bf16 patterns
+    c_b, k_b = oracle.cache_append(hb, wdb, wrb, [7, 8])
+    c_f, k_f = oracle.cache_append(from_bits(hb), from_bits(wdb), from_bits(wrb), [7, 8])
+    np.testing.assert_array_equal(c_b, c_f)
+    np.testing.assert_array_equal(k_b, k_f)
+    assert abs(c_b[0, 0] - (from_bits(wdb)[0] @ from_bits(hb)[0])) < 1e-12
