@@ -60,3 +60,36 @@ def test_static_scratch_limit_matches_the_header():
     with open(binding.HEADER_PATH) as f:
         m = re.search(r"MLA_STATIC_SCRATCH_BYTES\s*=\s*(\d+)\s*<<\s*(\d+)", f.read())
     assert m and int(m.group(1)) << int(m.group(2)) == binding.STATIC_SCRATCH_BYTES
+
+
+def test_cache_append_host_validation(lib):
+    nul, fake = ctypes.c_void_p(0), ctypes.c_void_p(1 << 20)  # fake: aligned, never dereferenced
+    big = 1 << 30
+    assert lib.mla_cache_append(nul, fake, fake, fake, fake, fake, 1, 1, 64, 4, None, fake, big, None) == 1
+    assert lib.mla_cache_append(fake, fake, fake, fake, fake, fake, 0, 1, 64, 4, None, fake, big, None) == 1
+    assert lib.mla_cache_append(fake, fake, fake, fake, fake, fake, 1, 2, 64, 1, None, fake, big, None) == 1
+    assert lib.mla_cache_append(fake, fake, fake, fake, fake, fake, 1, 1, 100, 4, None, fake, big, None) == 2
+    assert lib.mla_cache_append(fake, fake, fake, fake, fake, fake, 1, 1, 64, 4, None, fake, 16, None) == 3
+    assert lib.mla_cache_append(fake, fake, fake, fake, fake, fake, 1, 1, 64, 4, None,
+                                ctypes.c_void_p((1 << 20) + 64), big, None) == 3   # not 256-byte aligned
+    misaligned = ctypes.c_void_p((1 << 20) + 8)
+    assert lib.mla_cache_append(misaligned, fake, fake, fake, fake, fake, 1, 1, 64, 4, None, fake, big,
+                                None) == 1
+
+
+def test_cache_append_workspace_size(lib):
+    assert lib.mla_cache_append_workspace_size(1, 1, 100) == 0     # d not a multiple of 64
+    assert lib.mla_cache_append_workspace_size(0, 1, 64) == 0
+    # status word, then fp32 partial products [ceil(d / 256)][B * S][576], 256-byte rounded
+    n = 4 * 28 * 32 * 576
+    assert lib.mla_cache_append_workspace_size(32, 1, 7168) == 256 + (n + 255) // 256 * 256
+    assert lib.mla_cache_append_workspace_size(3, 2, 448) == 256 + (4 * 2 * 6 * 576 + 255) // 256 * 256
+
+
+def test_combine_up_project_host_validation(lib):
+    nul, fake = ctypes.c_void_p(0), ctypes.c_void_p(1 << 20)
+    assert lib.mla_combine_up_project(fake, 1 << 30, nul, fake, 1, 1, 1, None) == 1
+    assert lib.mla_combine_up_project(fake, 1 << 30, fake, fake, 0, 1, 1, None) == 1
+    assert lib.mla_combine_up_project(fake, 1 << 30, fake, fake, 1, 1, 200, None) == 2
+    assert lib.mla_combine_up_project(fake, 1 << 30, fake, fake, 1, 17, 128, None) == 2  # S*H > 2048
+    assert lib.mla_combine_up_project(nul, 1 << 30, fake, fake, 1, 1, 16, None) == 3
