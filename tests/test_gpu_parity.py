@@ -219,7 +219,7 @@ def test_decode_never_reads_unwritten_workspace():
     q, c, k, sl = _latent_case(3, 2, 96, [2, 700, 2500], seed=202)
     B, S, H = 3, 2, 96
     ws = mb.new_workspace(B, S, H)
-    ws[256:] = 0x3F                     # every fp32 partial reads as 0.747
+    ws[256:] = 0x3F                     # every (m, l) reads as 0.747, every fp16 partial as 1.81
     o = torch.empty(B, S, H, 512, dtype=torch.bfloat16, device="cuda")
     for _ in range(2):
         mb.decode(q.cuda(), c.cuda(), k.cuda(), sl.cuda(), ws)
