@@ -22,12 +22,11 @@
 // segments' partial rows (lanes over column octets), so a row with up to two
 // segments costs one memory round trip; the rest follow two segments at a
 // time.  The merged row is rounded to bf16 and written in the 128-byte
-// swizzled K-major layout the MMA reads; then the MMA and epilogue are those
-// of up_project.cuh.
+// swizzled K-major layout the MMA reads; then the MMA and epilogue follow
+// up_project.cuh.
 #pragma once
 
 #include "splitkv.cuh"
-#include "up_project.cuh"
 
 namespace mla {
 
