@@ -339,7 +339,7 @@ def run_ours(args, x, rank, world, local_rank):
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded; random-init weights of the pages' MLA dimensions)",
         "config": _config(args, x),
-        "roofline": {"kernel": "mla_decode (plan + decode kernels)", "bound": "hbm",
+        "roofline": {"kernel": "mla_decode (the decode kernel, which plans its own split)", "bound": "hbm",
                      "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(achieved / hbm, 4),
                      "traffic": _decode_traffic() if args.workload == DEFAULT_WORKLOAD else None,
