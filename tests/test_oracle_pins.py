@@ -107,13 +107,14 @@ def test_rope_relative_position_invariance():
 
 
 # ---------------------------------------------------------------- decode pins
-def test_decode_matches_sdpa_on_expanded_kv():
+@pytest.mark.parametrize("S,seqlens", [(2, [2, 6, 9]), (5, [5, 6, 10])])
+def test_decode_matches_sdpa_on_expanded_kv(S, seqlens):
     """Library cross-check: keys k = [W^UK c ; RoPE(k_R)] and values v = W^UV c
     expanded explicitly, then torch's scaled_dot_product_attention (float64)
-    with a causal mask whose query s sits at position L_b - S + s."""
-    rng = np.random.default_rng(5)
-    B, S, H, d_c, d_h, d_r, d_v = 3, 2, 3, 12, 5, 4, 7
-    seqlens = [2, 6, 9]
+    with a causal mask whose query s sits at position L_b - S + s (S = 5: a
+    prefill chunk, including a sequence exactly as long as its chunk)."""
+    rng = np.random.default_rng(5 + S)
+    B, H, d_c, d_h, d_r, d_v = 3, 3, 12, 5, 4, 7
     p = _rand_problem(rng, B, S, H, seqlens, d_c, d_h, d_r, d_v, Lmax=10)
     scale = 1.0 / math.sqrt(d_h + d_r)
     got = oracle.decode(p["q_nope"], p["q_rope"], p["c_kv"], p["k_r"], p["W_UK"], p["W_UV"],
