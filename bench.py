@@ -20,6 +20,7 @@ import math
 import os
 import statistics
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -90,7 +91,9 @@ class ClockSampler:
     def __init__(self, index: int):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+        # raw samples; the summary goes into the JSON line
+        log_dir = os.environ.get("MLA_BENCH_LOG_DIR", os.path.join(tempfile.gettempdir(), "mla_bench"))
+        self.path = os.path.join(log_dir, f"clocks_rank{index}.csv")
 
     def __enter__(self):
         try:
