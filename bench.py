@@ -143,8 +143,7 @@ def _oracle_sample(x, seconds: float, seed: int = 0, rope: str = "plain"):
     import oracle
     kw = {}
     if rope == "yarn":
-        kw = dict(rope_theta=oracle.yarn_theta(64),
-                  softmax_scale=(0.1 * math.log(40.0) + 1.0) / math.sqrt(192.0))
+        kw = dict(rope_theta=oracle.yarn_theta(64), softmax_scale=oracle.yarn_softmax_scale(40.0))
     threads = oracle.num_threads()
     b = {k: bf16_bits(x[k]) for k in ("q_nope", "q_rope", "c_kv", "k_r", "W_UK", "W_UV")}
     total = x["B"] * x["S"] * x["H"]

@@ -146,11 +146,21 @@ mla_status mla_absorb_rope_q_freq(const mla_bf16 *q_nope, const mla_bf16 *q_rope
  * clamped to [0, 1] between alpha and beta turns; theta_j = base^(-2j/64).
  * Host-only arithmetic; writes theta[0..31].  Returns MLA_OK or
  * MLA_ERR_INVALID_ARG.  Use the result for the queries' and the cache's RoPE
- * alike, and scale the scores by (0.1 ln s + 1): softmax_scale =
- * (0.1 ln s + 1) / sqrt(192) in mla_decode.
+ * alike, and pass mla_rope_yarn_softmax_scale(s) as mla_decode's softmax_scale.
  */
 int mla_rope_yarn_frequencies(double base, double s, double alpha, double beta, double orig_len,
                               double *theta);
+
+/*
+ * Softmax scale of the YaRN setting ("Long Context Extension" of the
+ * technical report: the scores are multiplied by 0.1 ln s + 1; "YaRN 扩展"
+ * applies the factor to the scores before the softmax):
+ *     *scale = (0.1 ln s + 1) / sqrt(d_h + d_h^R) = (0.1 ln s + 1) / sqrt(192).
+ * Host-only arithmetic in double precision.  Returns MLA_OK, or
+ * MLA_ERR_INVALID_ARG (and leaves *scale alone) if s < 1, s is not finite or
+ * scale is NULL.  s = 1 gives the plain 1/sqrt(192).
+ */
+int mla_rope_yarn_softmax_scale(double s, double *scale);
 
 /*
  * Bytes of device workspace mla_decode needs for this shape on the current

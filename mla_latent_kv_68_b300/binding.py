@@ -59,6 +59,7 @@ def lib():
         L.mla_rope_apply_freq.argtypes = [vp, i64, i64, vp, i64, i64, i64, i32, i32, vp, i32, vp, vp]
         f64 = ctypes.c_double
         L.mla_rope_yarn_frequencies.argtypes = [f64, f64, f64, f64, f64, vp]
+        L.mla_rope_yarn_softmax_scale.argtypes = [f64, vp]
         L.mla_rope_apply.argtypes = [vp, i64, i64, vp, i64, i64, i64, i32, i32, vp, i32, f32, vp]
         L.mla_decode_workspace_size.restype = sz
         L.mla_decode_workspace_size.argtypes = [i32, i32, i32]
@@ -72,7 +73,8 @@ def lib():
         L.mla_read_status.argtypes = [vp, vp]
         L.mla_decode_noalloc.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, f32, vp, vp]
         for n in ("mla_absorb_q", "mla_absorb_rope_q", "mla_absorb_rope_q_freq", "mla_rope_apply",
-                  "mla_rope_apply_freq", "mla_rope_yarn_frequencies", "mla_decode",
+                  "mla_rope_apply_freq", "mla_rope_yarn_frequencies", "mla_rope_yarn_softmax_scale",
+                  "mla_decode",
                   "mla_splitkv_combine", "mla_up_project", "mla_combine_up_project", "mla_read_status",
                   "mla_cache_append",
                   "mla_decode_noalloc"):
@@ -134,8 +136,11 @@ def yarn_frequencies(s=40.0, alpha=1.0, beta=32.0, orig_len=4096.0, base=ROPE_BA
 
 
 def yarn_softmax_scale(s=40.0):
-    """Score scale with YaRN's attention factor 0.1 ln s + 1 on 1/sqrt(192)."""
-    return (0.1 * math.log(s) + 1.0) * SOFTMAX_SCALE
+    """Softmax scale of the YaRN setting, from mla_rope_yarn_softmax_scale."""
+    out = ctypes.c_double()
+    _check(lib().mla_rope_yarn_softmax_scale(float(s), ctypes.byref(out)),
+           "mla_rope_yarn_softmax_scale")
+    return float(out.value)
 
 
 def _theta_arg(theta):

@@ -348,6 +348,12 @@ int mla_rope_yarn_frequencies(double base, double s, double alpha, double beta, 
   return MLA_OK;
 }
 
+int mla_rope_yarn_softmax_scale(double s, double* scale) {
+  if (!scale || !(s >= 1.0) || !std::isfinite(s)) return MLA_ERR_INVALID_ARG;
+  *scale = (0.1 * std::log(s) + 1.0) / std::sqrt((double)(MLA_D_H + MLA_D_R));
+  return MLA_OK;
+}
+
 mla_status mla_rope_apply(const mla_bf16* x_in, int64_t in_stride_n, int64_t in_stride_h,
                           mla_bf16* x_out, int64_t out_stride_n, int64_t out_stride_h, int64_t N,
                           int nh, int pos_mode, const int32_t* pos_src, int group, float base,

@@ -12,6 +12,7 @@ from .oracle import (  # noqa: F401
     rope,
     rope_theta,
     yarn_theta,
+    yarn_softmax_scale,
     decode,
     cache_append,
     absorb,

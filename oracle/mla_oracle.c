@@ -99,6 +99,18 @@ int mla_oracle_yarn_theta(double base, int d_r, double s, double alpha, double b
   return 0;
 }
 
+/*
+ * YaRN score factor ("Long Context Extension" of the technical report reading:
+ * the attention scores are scaled by 0.1 ln s + 1; "YaRN 扩展" applies it to the
+ * scores before the softmax): the softmax scale becomes
+ * (0.1 ln s + 1) / sqrt(d_h + d_r) in place of 1 / sqrt(d_h + d_r).
+ */
+int mla_oracle_yarn_softmax_scale(double s, int d_h, int d_r, double *out) {
+  if (!(s >= 1.0) || d_h <= 0 || d_r < 0 || !out) return 1;
+  *out = (0.1 * log(s) + 1.0) / sqrt((double)(d_h + d_r));
+  return 0;
+}
+
 /* RoPE of one d_r-vector at integer position pos ("YaRN 扩展": phi_{m,j} = m theta_j). */
 static void rope_vec(const double *x, int d_r, double pos, const double *theta, double *y) {
   for (int j = 0; j < d_r / 2; ++j) {

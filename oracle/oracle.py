@@ -43,6 +43,7 @@ def load():
         lib.mla_oracle_rope.argtypes = [vp, i32, vp, i32, i32, f64, vp]
         lib.mla_oracle_rope_theta.argtypes = [vp, i32, vp, i32, i32, vp, vp]
         lib.mla_oracle_yarn_theta.argtypes = [f64, i32, f64, f64, f64, f64, vp]
+        lib.mla_oracle_yarn_softmax_scale.argtypes = [f64, i32, i32, vp]
         lib.mla_oracle_decode_theta.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32,
                                                 i32, i32, i32, i32, i32, f64, vp, vp, i64, vp, vp]
         lib.mla_oracle_decode.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32,
@@ -53,7 +54,8 @@ def load():
                                                     i32, i32, f64, vp, i64, vp]
         for name in ("mla_oracle_rope", "mla_oracle_decode", "mla_oracle_absorb",
                      "mla_oracle_up_project", "mla_oracle_latent_attention",
-                     "mla_oracle_rope_theta", "mla_oracle_yarn_theta", "mla_oracle_decode_theta"):
+                     "mla_oracle_rope_theta", "mla_oracle_yarn_theta", "mla_oracle_decode_theta",
+                     "mla_oracle_yarn_softmax_scale"):
             getattr(lib, name).restype = i32
         _lib = lib
     return _lib
@@ -113,6 +115,15 @@ def yarn_theta(d_r: int = 64, *, base: float = 10000.0, s: float = 40.0, alpha: 
     _check(load().mla_oracle_yarn_theta(float(base), d_r, float(s), float(alpha), float(beta),
                                         float(orig_len), _ptr(out)), "yarn_theta")
     return out
+
+
+def yarn_softmax_scale(s: float = 40.0, d_h: int = 128, d_r: int = 64) -> float:
+    """Softmax scale with YaRN's score factor, (0.1 ln s + 1) / sqrt(d_h + d_r)
+    ("Long Context Extension"; "YaRN 扩展" scales the scores before the softmax)."""
+    out = ctypes.c_double()
+    _check(load().mla_oracle_yarn_softmax_scale(float(s), int(d_h), int(d_r), ctypes.byref(out)),
+           "yarn_softmax_scale")
+    return float(out.value)
 
 
 def rope_theta(x, pos, theta):

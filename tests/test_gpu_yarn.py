@@ -76,15 +76,17 @@ def _oracle_rows(x, th, scale, rows=None):
 
 
 def test_whole_step_with_yarn_matches_unabsorbed_oracle():
-    th, scale = _yarn(), mb.yarn_softmax_scale(40.0)
+    # the GPU step takes the library's frequencies and scale, the oracle its own
     x = make_inputs(3, 2, 8, [2, 300, 5000], seed=23)
-    assert_close(_yarn_step(x, th, scale), _oracle_rows(x, th, scale), what="yarn step")
+    got = _yarn_step(x, mb.yarn_frequencies(), mb.yarn_softmax_scale(40.0))
+    assert_close(got, _oracle_rows(x, oracle.yarn_theta(64), oracle.yarn_softmax_scale(40.0)),
+                 what="yarn step")
 
 
 def test_long_workload_with_yarn_sampled_rows():
-    th, scale = _yarn(), mb.yarn_softmax_scale(40.0)
     x = workload_inputs("long_b4_s1_h128_l131072")
-    got = _yarn_step(x, th, scale).reshape(-1, 128)
+    got = _yarn_step(x, mb.yarn_frequencies(), mb.yarn_softmax_scale(40.0)).reshape(-1, 128)
     rows = np.array([0, 127, 128 + 5, 2 * 128 + 64, 3 * 128 + 127], np.int64)
-    assert_close(got[rows], _oracle_rows(x, th, scale, rows=rows), what="yarn 128K")
+    ref = _oracle_rows(x, oracle.yarn_theta(64), oracle.yarn_softmax_scale(40.0), rows=rows)
+    assert_close(got[rows], ref, what="yarn 128K")
     torch.cuda.empty_cache()

@@ -117,7 +117,7 @@ def test_decode_with_yarn_matches_sdpa_on_expanded_kv():
     k_r = rng.standard_normal((B, Lmax, d_r))
     W_UK = rng.standard_normal((H, d_h, d_c)) / math.sqrt(d_c)
     W_UV = rng.standard_normal((H, d_v, d_c)) / math.sqrt(d_c)
-    scale = (0.1 * math.log(40.0) + 1.0) / math.sqrt(d_h + d_r)
+    scale = oracle.yarn_softmax_scale(40.0, d_h, d_r)
     got = oracle.decode(q_nope, q_rope, c_kv, k_r, W_UK, W_UV, np.array(seqlens, np.int32),
                         softmax_scale=scale, rope_theta=yt)
     for b in range(B):
@@ -136,3 +136,17 @@ def test_decode_with_yarn_matches_sdpa_on_expanded_kv():
             torch.from_numpy(np.ascontiguousarray(V)), attn_mask=torch.from_numpy(mask),
             scale=scale).numpy()
         np.testing.assert_allclose(got[b], ref.transpose(1, 0, 2), rtol=1e-11, atol=1e-12)
+
+
+def test_yarn_score_factor_closed_forms():
+    # "Long Context Extension": the scores are scaled by 0.1 ln s + 1 on top of
+    # 1/sqrt(d_h + d_r).  s = 1 is plain attention; s = e^10 doubles the scale;
+    # the factor grows with s; d_h + d_r = 192 for the pages' model.
+    assert oracle.yarn_softmax_scale(1.0, 128, 64) == 1.0 / math.sqrt(192.0)
+    assert oracle.yarn_softmax_scale(math.exp(10.0), 128, 64) == pytest.approx(2.0 / math.sqrt(192.0),
+                                                                              rel=1e-15)
+    assert oracle.yarn_softmax_scale(40.0, 128, 64) == pytest.approx(1.3688879454113936 / math.sqrt(192.0),
+                                                                     rel=1e-15)
+    assert oracle.yarn_softmax_scale(40.0, 3, 1) == pytest.approx(1.3688879454113936 / 2.0, rel=1e-15)
+    with pytest.raises(ValueError):
+        oracle.yarn_softmax_scale(0.5)

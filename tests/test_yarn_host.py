@@ -32,8 +32,17 @@ def test_yarn_frequencies_reject_bad_arguments(lib):
     assert lib.mla_rope_yarn_frequencies(10000.0, 40.0, 1.0, 32.0, 4096.0, None) == 1
 
 
-def test_yarn_softmax_scale():
-    assert binding.yarn_softmax_scale(40.0) == pytest.approx((0.1 * math.log(40.0) + 1.0) / math.sqrt(192))
+@pytest.mark.parametrize("s", [1.0, 2.0, 40.0, 1e6])
+def test_library_yarn_softmax_scale_matches_oracle(lib, s):
+    assert binding.yarn_softmax_scale(s) == pytest.approx(oracle.yarn_softmax_scale(s), rel=1e-15)
+
+
+def test_yarn_softmax_scale_rejects_bad_arguments(lib):
+    out = ctypes.c_double(-1.0)
+    for s in (0.5, float("nan"), float("inf")):
+        assert lib.mla_rope_yarn_softmax_scale(s, ctypes.byref(out)) == 1
+    assert out.value == -1.0
+    assert lib.mla_rope_yarn_softmax_scale(40.0, None) == 1
 
 
 def test_freq_entries_reject_bad_frequencies(lib):
