@@ -85,55 +85,58 @@ constexpr int kTok = kTileRows;   // cache rows per tile (128)
 constexpr int kBlk0 = kTok * 128;          // one block: 128 rows x 64 bf16 = 16 KB
 constexpr int kCStage = 4 * kBlk0;         // c ring stage: four blocks (one 64 KB TMA box)
 constexpr int kCStages = 2;
+constexpr int kCPerTile = 2;               // c stages per 128-row tile (512 columns)
 constexpr int kRStage = kBlk0;             // k^R ring stage: one block (16 KB)
 constexpr int kRStages = 2;
 constexpr int kOffR = kCStages * kCStage;  // k^R ring
 constexpr int kOffQR = kOffR + kRStages * kRStage;  // q^R of the segment: 128 x 64 bf16 (A of the RoPE MMAs)
-constexpr int kOffPS = kOffQR + kBlk0;     // P staging: 128 x 128 bf16 + rescale exponents[128] + row sums
-constexpr int kPBytes = 128 * kTok * 2;
-constexpr int kOffPL = kPBytes + 128;         // in a P slot: row sums l (f32 [128]) after the exponents
-constexpr uint32_t kPTx = kOffPL + 512;       // bytes of one P slot: P, rescale exponents, row sums
-constexpr int kOffXch = kOffPS + (int)kPTx;   // ceil(row max) int16 [2 tiles][2 halves][128], row sum f32 [128]
+constexpr int kOffXch = kOffQR + kBlk0;    // ceil(row max) int16 [2 tiles][2 halves][128], row sum f32 [128]
 constexpr int kXchBytes = 2 * 2 * 128 * 2 + 128 * 4;
+// a P slot of the value CTA: P (128 x 128 bf16), rescale exponents u32 [128], row sums f32 [128]
+constexpr int kPBytes = 128 * kTok * 2;
+constexpr int kOffPEx = kPBytes;
+constexpr int kOffPL = kOffPEx + 128 * 4;
+constexpr uint32_t kPTx = kOffPL + 128 * 4;   // bytes the score CTA stores into one P slot
 // value CTA (rank 1)
-constexpr int kSub = 64;                   // cache rows per value-CTA stage
-constexpr int kBlk1 = kSub * 128;          // 8 KB
-constexpr int kStage1 = 8 * kBlk1;         // 64 KB: one TMA box (fewer, larger boxes)
-constexpr int kStages1 = 2;
+constexpr int kSub = 32;                   // cache rows per value-CTA stage
+constexpr int kBlk1 = kSub * 128;          // 4 KB
+constexpr int kStage1 = 8 * kBlk1;         // 32 KB: one TMA box of whole 1 KB rows
+constexpr int kStages1 = 5;
 constexpr int kStepsPerSub = kSub / 16;    // P . C K-steps per value-CTA stage
 constexpr int kOffP = kStages1 * kStage1;  // P slots [2], each P then alpha
+// ring barriers of a CTA: the score CTA's c and k^R rings, or the value CTA's ring
+constexpr int kRingSlots = (kCStages + kRStages) > kStages1 ? (kCStages + kRStages) : kStages1;
 constexpr int kPSlot = 33 * 1024;          // slot stride (keeps P 1 KB aligned)
+static_assert(kPTx == (uint32_t)kPSlot, "a P slot is exactly what the score CTA stores into it");
 // shared by both
 constexpr int kEnd0 = kOffXch + kXchBytes, kEnd1 = kOffP + 2 * kPSlot;
 constexpr int kOffBar = kEnd0 > kEnd1 ? kEnd0 : kEnd1;
-constexpr int kNumBars = 49;
+constexpr int kNumBars = 47;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tensor-memory address, abort flag
 constexpr int kOffPlan = kOffMisc + 16;            // PlanState
 constexpr int kDecSmem = kOffPlan + 32;
 static_assert(kDecSmem <= 232448, "decode shared memory exceeds 227 KB");
-static_assert(kOffQR % 1024 == 0 && kOffPS % 1024 == 0 && kOffP % 1024 == 0 && kPSlot % 1024 == 0,
+static_assert(kRingSlots <= 10, "the FULL / EMPTY barrier ranges hold 10 ring slots each");
+static_assert(kOffR % 1024 == 0 && kOffQR % 1024 == 0 && kOffP % 1024 == 0 && kPSlot % 1024 == 0,
               "swizzled operands need 1 KB alignment");
-static_assert(kPTx % 16 == 0 && kPTx <= (uint32_t)kPSlot,
-              "P slot layout");
-constexpr uint32_t kQCol = 256;   // score CTA: q~ at tensor-memory columns 256..511; S buffers at 0, 128
+// score CTA tensor memory: S buffers at columns 0..127 and 128..255, q~ at 256..511
+constexpr uint32_t kQCol = 256;
 
 // barrier indices
 enum : int {
-  B_FULL = 0, B_EMPTY = 10,          // TMA rings (rank 0: c at 0..1, k^R at 2..3; rank 1: 0..1)
+  B_FULL = 0, B_EMPTY = 10,          // TMA rings (rank 0: c, then k^R; rank 1: its c ring), kRingSlots each
   B_SFULL = 20, B_SEMPTY = 22,       // score CTA: the two S buffers
   B_PEMPTY = 24,                     // score CTA: P slot in the value CTA free again
-  B_XCH = 27,                        // score CTA: row-max exchange [tile parity][quadrant]
-  B_XL = 35,                         // score CTA: row-sum exchange at a segment end
-  B_PSTAGED = 36,                    // score CTA: P of a tile is in the staging buffer
-  B_PSFREE = 37,                     // score CTA: staging buffer read by the copy
-  B_PFULL = 38,                      // value CTA: P + alpha of a tile have arrived
-  B_PREADY = 40,                     // value CTA: O rescaled, P may be consumed
-  B_PVDONE = 42,                     // value CTA: P . C of a tile completed
-  B_OFREE = 44,                      // value CTA: epilogue has read O
-  B_DRAIN = 45,                      // both: final MMA drain
-  B_QRFULL = 46,                     // score CTA: q^R of the segment has landed
-  B_QREMPTY = 47,                    // score CTA: the segment's MMAs no longer read q^R
-  B_PLAN = 48                        // both: the split plan of this CTA's group is in PlanState
+  B_XCH = 26,                        // score CTA: row-max exchange [tile parity][quadrant]
+  B_XL = 34,                         // score CTA: row-sum exchange at a segment end
+  B_PFULL = 35,                      // value CTA: P + alpha of a tile have arrived
+  B_PREADY = 37,                     // value CTA: O rescaled, P may be consumed
+  B_PVDONE = 39,                     // value CTA: P . C of a tile completed
+  B_OFREE = 41,                      // value CTA: epilogue has read O
+  B_DRAIN = 42,                      // both: final MMA drain
+  B_QRFULL = 43,                     // score CTA: q^R of the segment has landed
+  B_QREMPTY = 44,                    // score CTA: the segment's MMAs no longer read q~ and q^R
+  B_PLAN = 45                        // both: the split plan of this CTA's group is in PlanState
 };
 
 struct DecodeParams {
@@ -148,7 +151,48 @@ struct DecodeParams {
   int B, S, H, Lmax, n_rb, G;
   float scale_log2;            // softmax_scale * log2(e)
   uint64_t timeout_ns;
+  unsigned long long* trace;   // timeline of a diagnostic build (MLA_DECODE_TRACE), else unused
 };
+
+// Diagnostic timeline: with MLA_DECODE_TRACE defined, the kernel stamps the
+// global timer at fixed points of each tile into
+// trace[cluster][event][tile] (first kTraceSlots tiles or segments).  The
+// product build compiles the stamps away.
+constexpr int kTraceEvents = 24, kTraceSlots = 64;
+enum : int {
+  TR_START = 0,       // kernel entry (rank 0, thread 0)           [slot 0]
+  TR_PLAN = 1,        // plan ready (rank 0, plan warp)             [slot 0]
+  TR_TMA_ISSUE = 2,   // score CTA: first c stage of the tile issued
+  TR_QK_BEGIN = 3,    // score CTA: first QK^T MMA of the tile issued
+  TR_QK_END = 4,      // score CTA: last QK^T MMA of the tile issued
+  TR_S_READY = 5,     // score CTA: a softmax thread saw S
+  TR_P_SENT = 6,      // score CTA: that thread has issued its P stores
+  TR_P_FULL = 7,      // value CTA: a row thread saw the P slot full
+  TR_PV_BEGIN = 8,    // value CTA: first P . C MMA issued
+  TR_PV_END = 9,      // value CTA: last P . C MMA issued
+  TR_PV_DONE = 10,    // value CTA: P . C completed (releaser)
+  TR_EPI_BEGIN = 11,  // value CTA: epilogue of a segment begins      [segment]
+  TR_EPI_END = 12,    // value CTA: epilogue stores issued            [segment]
+  TR_END = 13,        // wind-down reached (rank 0 / rank 1)          [slot rank]
+  TR_V_TMA = 14,      // value CTA: first c stage of the tile issued
+  TR_SM_MAX = 15,     // score CTA: that softmax thread has its row maximum
+  TR_SM_XCH = 16,     // score CTA: ... and its partner's
+  TR_SM_SLOT = 17,    // score CTA: ... and the P slot is free
+  TR_QK_LAST = 18,    // score CTA: the tile's last c stage has landed (MMA thread)
+  TR_V_LAND = 19      // value CTA: the tile's last c stage has landed (MMA thread)
+};
+#ifdef MLA_DECODE_TRACE
+#define MLA_TRACE(p, ev, idx)                                                                   \
+  do {                                                                                          \
+    if ((p).trace && (idx) < kTraceSlots)                                                       \
+      (p).trace[((size_t)(blockIdx.x >> 1) * kTraceEvents + (ev)) * kTraceSlots + (idx)] =       \
+          global_timer_ns();                                                                    \
+  } while (0)
+#else
+#define MLA_TRACE(p, ev, idx) \
+  do {                        \
+  } while (0)
+#endif
 
 struct TileInfo {
   int b, t, L, i, k, slot;
@@ -339,8 +383,8 @@ __device__ __forceinline__ void for_each_tile_warm(const DecodeParams& p, int g,
 // sends its 512 q~ columns through the c ring (two stages), every tile its
 // cache rows (the same); c stage h holds blocks 4h .. 4h + 3.  The k^R ring
 // carries cache rows only (tile i at position i); q^R has its own buffer.
-__device__ __forceinline__ int cpos_q(int i, int k, int h) { return 2 * (i + k) + h; }
-__device__ __forceinline__ int cpos_kv(int i, int k, int h) { return 2 * (i + k + 1) + h; }
+__device__ __forceinline__ int cpos_q(int i, int k, int h) { return kCPerTile * (i + k) + h; }
+__device__ __forceinline__ int cpos_kv(int i, int k, int h) { return kCPerTile * (i + k + 1) + h; }
 constexpr int kBarC = 0, kBarR = kCStages;  // FULL / EMPTY sub-ranges of the two rings
 
 // All 32 lanes wait; the outcome is made warp-uniform so that warp-collective
@@ -370,12 +414,13 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   const WaitCtx wc{abort_flag, p.status, p.timeout_ns};
 
   if (threadIdx.x == 0) {
+    if (rank == 0) MLA_TRACE(p, TR_START, 0);
     *abort_flag = 0u;
     if (smem_u32(smem) & 1023u) {  // the swizzled tiles need 1 KB alignment
       *abort_flag = 1u;
       atomicOr(p.status, kDevErrInternal);
     }
-    for (int s = 0; s < kCStages + kRStages; ++s) {
+    for (int s = 0; s < kRingSlots; ++s) {
       mbar_init(&bar[B_FULL + s], 1);
       mbar_init(&bar[B_EMPTY + s], 1);
     }
@@ -389,8 +434,6 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     }
     for (int s = 0; s < 8; ++s) mbar_init(&bar[B_XCH + s], 64);
     mbar_init(&bar[B_XL], 256);
-    mbar_init(&bar[B_PSTAGED], 256);
-    mbar_init(&bar[B_PSFREE], 1);
     mbar_init(&bar[B_OFREE], 256);
     mbar_init(&bar[B_DRAIN], 1);
     mbar_init(&bar[B_QRFULL], 1);
@@ -427,6 +470,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     pdl_wait();
     plan_scan(p, g, blockIdx.x == 0, plan);
     __syncwarp();
+    if (lane == 0 && rank == 0) MLA_TRACE(p, TR_PLAN, 0);
     if (lane == 0) mbar_arrive(&bar[B_PLAN]);
   } else if (!rows) {
     pdl_wait();
@@ -437,9 +481,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   if (run && warp == 0) {
     // ------------------------------------------------ TMA producer (both CTAs)
     if (lane == 0) {
-      int last_use[kCStages + kRStages];
-      for (int s = 0; s < kCStages + kRStages; ++s) last_use[s] = -1;
       int qr_last = -1;  // last segment whose q^R was loaded
+      int last_use[kRingSlots];
+      for (int s = 0; s < kRingSlots; ++s) last_use[s] = -1;
       int cq = 0, rq = 0, q = 0;  // running positions: score c ring, score k^R ring, value ring
       // Issue one stage of a ring: wait for the slot, arm its barrier, copy.
       auto slot = [&](int base, int nst, int pos, uint32_t bytes) -> int {
@@ -454,7 +498,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         if (rank == 0) {
           if (ti.first) {  // the segment's query rows: blocks 0..7 through the c ring, q^R to its buffer
             const int qrow0 = ti.b * SH + rb * 128;
-            for (int h = 0; h < 2; ++h, ++cq) {
+            for (int h = 0; h < kCPerTile; ++h, ++cq) {
               const int st = slot(kBarC, kCStages, cq, kCStage);
               if (st < 0) return false;
               tma_load_3d(smem + st * kCStage, &tm_q, &bar[B_FULL + kBarC + st], 0, qrow0, 4 * h);
@@ -464,9 +508,10 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             qr_last = ti.k;
             tma_load_2d(smem + kOffQR, &tm_qr, &bar[B_QRFULL], 512, qrow0);
           }
-          for (int h = 0; h < 2; ++h, ++cq) {
+          for (int h = 0; h < kCPerTile; ++h, ++cq) {
             const int st = slot(kBarC, kCStages, cq, kCStage);
             if (st < 0) return false;
+            if (h == 0) MLA_TRACE(p, TR_TMA_ISSUE, ti.i);
             tma_load_3d(smem + st * kCStage, &tm_c0, &bar[B_FULL + kBarC + st], 0, row0, 4 * h);
           }
           const int st = slot(kBarR, kRStages, rq++, kRStage);
@@ -477,13 +522,14 @@ __global__ void __launch_bounds__(kDecThreads, 1)
           for (int u = 0; u < nsub; ++u, ++q) {  // 64-row stages of the 512 c columns
             const int st = slot(0, kStages1, q, kStage1);
             if (st < 0) return false;
+            if (u == 0) MLA_TRACE(p, TR_V_TMA, ti.i);
             tma_load_3d(smem + st * kStage1, &tm_c1, &bar[B_FULL + st], 0, row0 + u * kSub, 0);
           }
         }
         return true;
       });
       // let every issued copy land before the CTA winds down
-      for (int s = 0; s < kCStages + kRStages; ++s) {
+      for (int s = 0; s < kRingSlots; ++s) {
         if (last_use[s] < 0) continue;
         const int nst = rank == 0 ? (s < kBarR ? kCStages : kRStages) : kStages1;
         mbar_wait_drain(&bar[B_FULL + s], (uint32_t)(last_use[s] / nst) & 1u, wc);
@@ -504,7 +550,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             // the old q~) has completed; the copy is ordered before this
             // thread's next MMAs.  q^R must have landed in its buffer.
             if (ti.k > 0 && !mbar_wait(&bar[B_QREMPTY], (uint32_t)(ti.k - 1) & 1u, wc)) return false;
-            for (int h = 0; h < 2; ++h) {
+            for (int h = 0; h < kCPerTile; ++h) {
               const int q = cpos_q(ti.i, ti.k, h), st = q % kCStages;
               if (!mbar_wait(&bar[B_FULL + kBarC + st], (uint32_t)(q / kCStages) & 1u, wc)) return false;
               tc_fence_after();
@@ -519,11 +565,13 @@ __global__ void __launch_bounds__(kDecThreads, 1)
           }
           if (!mbar_wait(&bar[B_SEMPTY + sb], sph ^ 1u, wc)) return false;
           const uint32_t d = tmem + (uint32_t)sb * 128u;
-          for (int h = 0; h < 2; ++h) {  // c blocks 4h .. 4h + 3 against q~ from tensor memory
+          for (int h = 0; h < kCPerTile; ++h) {  // c blocks 2h, 2h + 1 against q~ from tensor memory
             const int q = cpos_kv(ti.i, ti.k, h), st = q % kCStages;
             if (!mbar_wait(&bar[B_FULL + kBarC + st], (uint32_t)(q / kCStages) & 1u, wc)) return false;
+            if (h == kCPerTile - 1) MLA_TRACE(p, TR_QK_LAST, ti.i);
             tc_fence_after();
             const uint32_t sbase = smem_u32(smem + st * kCStage);
+            if (h == 0) MLA_TRACE(p, TR_QK_BEGIN, ti.i);
 #pragma unroll
             for (int kk = 0; kk < 16; ++kk) {  // 4 blocks x 4 K-steps of 16
               const int gk = h * 16 + kk;
@@ -542,8 +590,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
               mma_ss(d, smem_desc(qbase + kk * 32, 16, 1024, 2), smem_desc(sbase + kk * 32, 16, 1024, 2), idesc, 1u);
             mma_commit(&bar[B_EMPTY + kBarR + st]);
           }
-          if (ti.last) mma_commit(&bar[B_QREMPTY]);  // the buffer may take the next segment's q^R
+          if (ti.last) mma_commit(&bar[B_QREMPTY]);  // the next segment may replace q~ and q^R
           mma_commit(&bar[B_SFULL + sb]);
+          MLA_TRACE(p, TR_QK_END, ti.i);
           return true;
         });
       } else {
@@ -556,11 +605,13 @@ __global__ void __launch_bounds__(kDecThreads, 1)
           if (ti.first && ti.k > 0 && !mbar_wait(&bar[B_OFREE], (uint32_t)(ti.k - 1) & 1u, wc))
             return false;
           fence_proxy_async_cta();  // tail rows were zeroed through the generic proxy
+          MLA_TRACE(p, TR_PV_BEGIN, ti.i);
           const int nk = (ti.nvt + 15) >> 4;  // K-steps of 16 tokens
           const uint32_t pbase = smem_u32(smem + kOffP + slot * kPSlot);
           for (int u = 0; u * kStepsPerSub < nk; ++u, ++q) {
             const int st = q % kStages1;
             if (!mbar_wait(&bar[B_FULL + st], (uint32_t)(q / kStages1) & 1u, wc)) return false;
+            MLA_TRACE(p, TR_V_LAND, ti.i);
             tc_fence_after();
             const uint32_t sbase = smem_u32(smem + st * kStage1);
             for (int kt = 0; kt < kStepsPerSub && u * kStepsPerSub + kt < nk; ++kt) {
@@ -575,39 +626,23 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             mma_commit(&bar[B_EMPTY + st]);
           }
           mma_commit(&bar[B_PVDONE + slot]);
+          MLA_TRACE(p, TR_PV_END, ti.i);
           return true;
         });
       }
       mma_commit(&bar[B_DRAIN]);  // every MMA has finished before tensor memory is released
       mbar_wait_drain(&bar[B_DRAIN], 0, wc);
     }
-  } else if (run && warp == 2) {
+  } else if (run && warp == 2 && rank == 1) {
     if (lane == 0) {
-      if (rank == 0) {
-        // -------------------------------------------- score CTA: P copy into the value CTA
-        const uint32_t p_remote = map_to_cta(smem_u32(smem + kOffP), 1);
-        const uint32_t pfull_remote = map_to_cta(smem_u32(&bar[B_PFULL]), 1);
-        for_each_tile(p, g, *plan, [&](const TileInfo& ti) {
-          const int slot = ti.i & 1;
-          const uint32_t sph = (uint32_t)(ti.i >> 1) & 1u;
-          if (!mbar_wait(&bar[B_PSTAGED], (uint32_t)ti.i & 1u, wc)) return false;
-          if (!mbar_wait(&bar[B_PEMPTY + slot], sph ^ 1u, wc)) return false;
-          bulk_copy_to_peer(p_remote + (uint32_t)(slot * kPSlot), smem + kOffPS, kPTx,
-                            pfull_remote + (uint32_t)slot * 8);
-          bulk_commit_group();
-          bulk_wait_group_read0();
-          mbar_arrive(&bar[B_PSFREE]);
-          return true;
-        });
-      } else {
-        // -------------------------------------------- value CTA: P-slot releaser
-        for_each_tile(p, g, *plan, [&](const TileInfo& ti) {
-          const int slot = ti.i & 1;
-          if (!mbar_wait(&bar[B_PVDONE + slot], (uint32_t)(ti.i >> 1) & 1u, wc)) return false;
-          mbar_arrive_remote(&bar[B_PEMPTY + slot], 0);
-          return true;
-        });
-      }
+      // -------------------------------------------- value CTA: P-slot releaser
+      for_each_tile(p, g, *plan, [&](const TileInfo& ti) {
+        const int slot = ti.i & 1;
+        if (!mbar_wait(&bar[B_PVDONE + slot], (uint32_t)(ti.i >> 1) & 1u, wc)) return false;
+        MLA_TRACE(p, TR_PV_DONE, ti.i);
+        mbar_arrive_remote(&bar[B_PEMPTY + slot], 0);
+        return true;
+      });
     }
   } else if (run && warp >= 4) {
     // ------------------------------------------------ warps 4..11: two threads per row
@@ -623,7 +658,11 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       // ---------------------------------------- scores + online softmax
       int16_t* xch = reinterpret_cast<int16_t*>(smem + kOffXch);          // [2][2][128]
       float* xl = reinterpret_cast<float*>(smem + kOffXch + 2 * 2 * 128 * 2);  // [128]
-      uint8_t* ps = smem + kOffPS;
+      // P, the rescale exponent and the row sum go straight into the value
+      // CTA's P slot as asynchronous remote stores, each counted (in bytes) on
+      // that slot's barrier there.
+      const uint32_t p_remote = map_to_cta(smem_u32(smem + kOffP), 1);
+      const uint32_t pfull_remote = map_to_cta(smem_u32(&bar[B_PFULL]), 1);
       float m_ref = -INFINITY, l = 0.f;
       int limit = 0;
       for_each_tile_warm(p, g, *plan, &bar[B_PLAN], wc, [&](const TileInfo& ti) {
@@ -632,17 +671,19 @@ __global__ void __launch_bounds__(kDecThreads, 1)
           m_ref = -INFINITY;
           l = 0.f;
         }
-        const int slot = ti.i & 1;  // S buffer and exchange slot of this tile
+        const int slot = ti.i & 1;  // S buffer, exchange slot and P slot of this tile
         const uint32_t sph = (uint32_t)(ti.i >> 1) & 1u;
         if (!ti.dry && !warp_wait(&bar[B_SFULL + slot], sph, wc)) return false;
+        if (!ti.dry && threadIdx.x == 128) MLA_TRACE(p, TR_S_READY, ti.i);
         tc_fence_after();
         const uint32_t sc = tl + (uint32_t)(slot * 128 + hf * 64);  // this thread's 64 score columns
         const int nv = min(max(limit - ti.t * kTok - hf * 64, 0), 64);
 
         // The scores are read from tensor memory twice, 16 at a time, in
-        // rolled loops: the code stays small (its first run is bound by
-        // instruction fetch), and the other S buffer lets the next tile's
-        // QK^T run meanwhile.
+        // rolled loops: the code stays small (the instruction stream of the
+        // row warps competes with the other roles' for the SM's instruction
+        // caches), and the other S buffer lets the next tile's QK^T run
+        // meanwhile.
         float mx = -INFINITY;  // max of the raw scores; the scale is positive
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
@@ -654,6 +695,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             if (c * 16 + u < nv) mx = fmaxf(mx, __uint_as_float(v[u]));
         }
         mx *= p.scale_log2;
+        if (!ti.dry && threadIdx.x == 128) MLA_TRACE(p, TR_SM_MAX, ti.i);
         // Both threads of the row (same quadrant, warps q4 and q4 + 4) need the
         // same new reference exponent, which depends on the row maximum only
         // through ceil(max): for an integer m, max > m + 8 iff ceil(max) > m + 8.
@@ -664,6 +706,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
           mbar_arrive(&bar[B_XCH + slot * 4 + q4]);
           if (!warp_wait(&bar[B_XCH + slot * 4 + q4], sph, wc)) return false;
         }
+        if (!ti.dry && threadIdx.x == 128) MLA_TRACE(p, TR_SM_XCH, ti.i);
         const int cmax = max(cm, (int)xch[(slot * 2 + (hf ^ 1)) * 128 + r]);
         int ex = 0;  // rescale 2^-ex of O and l; 255 stands for 0
         if (cmax > -32768 && (float)cmax > m_ref + 8.f) {
@@ -674,9 +717,11 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         }
         const float mu = (m_ref == -INFINITY) ? 0.f : m_ref;
 
-        // the staging buffer is free once the previous tile's copy has read it
-        if (!ti.dry && !warp_wait(&bar[B_PSFREE], ((uint32_t)ti.i & 1u) ^ 1u, wc)) return false;
-        uint8_t* row = ps + hf * 16384 + r * 128;
+        // the value CTA's P slot is free once its P . C of two tiles ago completed
+        if (!ti.dry && !warp_wait(&bar[B_PEMPTY + slot], sph ^ 1u, wc)) return false;
+        if (!ti.dry && threadIdx.x == 128) MLA_TRACE(p, TR_SM_SLOT, ti.i);
+        const uint32_t pslot = p_remote + (uint32_t)(slot * kPSlot), pbar = pfull_remote + (uint32_t)slot * 8;
+        const uint32_t prow = pslot + (uint32_t)(hf * 16384 + r * 128);
         float lsum0 = 0.f, lsum1 = 0.f;
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {  // 2^(s scale log2 e - m), 16 columns per pass
@@ -696,11 +741,14 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             lsum1 += __high2float(b2);
           }
           // 128-byte swizzle: chunk ch of row r sits at ch ^ (r & 7)
-          *reinterpret_cast<uint4*>(row + (((2 * c) ^ (r & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          *reinterpret_cast<uint4*>(row + (((2 * c + 1) ^ (r & 7)) << 4)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+          if (!ti.dry) {
+            st_async_v4(prow + (uint32_t)(((2 * c) ^ (r & 7)) << 4), pk[0], pk[1], pk[2], pk[3], pbar);
+            st_async_v4(prow + (uint32_t)(((2 * c + 1) ^ (r & 7)) << 4), pk[4], pk[5], pk[6], pk[7], pbar);
+          }
         }
         tc_fence_before();
         if (!ti.dry) mbar_arrive(&bar[B_SEMPTY + slot]);  // this S buffer has been read
+        if (!ti.dry && threadIdx.x == 128) MLA_TRACE(p, TR_P_SENT, ti.i);
         l += lsum0 + lsum1;
         float l_seg = 0.f;  // segment end: the row's whole sum (both halves), for hf = 0
         if (ti.last && !ti.dry) {
@@ -711,13 +759,11 @@ __global__ void __launch_bounds__(kDecThreads, 1)
           // the next segment's exchange reuses xl only after its own tiles'
           // row-max exchanges, which both threads pass after reading it here
         }
-        if (hf == 0) {
-          ps[kPBytes + r] = (uint8_t)ex;
-          reinterpret_cast<float*>(ps + kOffPL)[r] = l_seg;  // the value CTA normalises O with it
-        }
-        fence_proxy_async_cta();  // the bulk copy reads the buffer through the async proxy
         if (ti.dry) return true;
-        mbar_arrive(&bar[B_PSTAGED]);
+        if (hf == 0) {  // the value CTA rescales O with ex and normalises it with l at a segment end
+          st_async_b32(pslot + (uint32_t)(kOffPEx + r * 4), (uint32_t)ex, pbar);
+          st_async_b32(pslot + (uint32_t)(kOffPL + r * 4), __float_as_uint(l_seg), pbar);
+        }
         if (ti.last && hf == 0 && valid)  // segment end: (m, l) of the row
           p.ml[((size_t)ti.slot * p.n_rb + rb) * 128 + r] = make_float2(mu, l_seg);
         return true;
@@ -733,7 +779,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         const int q0 = q;
         if (!ti.dry) q += nsub;
         if (!ti.dry && !warp_wait(&bar[B_PFULL + slot], sph, wc)) return false;
-        const int ex = reinterpret_cast<const volatile uint8_t*>(smem + kOffP + slot * kPSlot + kPBytes)[r];
+        if (!ti.dry && wt == 0) MLA_TRACE(p, TR_P_FULL, ti.i);
+        const int ex = (int)reinterpret_cast<const volatile uint32_t*>(smem + kOffP + slot * kPSlot + kOffPEx)[r];
         const float l_seg = ti.last
             ? reinterpret_cast<const volatile float*>(smem + kOffP + slot * kPSlot + kOffPL)[r] : 0.f;
         const float alpha = ex == 255 ? 0.f : exp2_int(-ex);
@@ -776,6 +823,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         mbar_arrive(&bar[B_PREADY + slot]);
         if (ti.last) {
           if (!warp_wait(&bar[B_PVDONE + slot], sph, wc)) return false;
+          if (wt == 0) MLA_TRACE(p, TR_EPI_BEGIN, ti.k);
           tc_fence_after();
           // O / l in fp16 as [64 column octets][128 rows] of 16 bytes: each
           // store of a warp covers 32 consecutive rows, 512 contiguous bytes.
@@ -803,6 +851,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             }
           }
           tc_fence_before();
+          if (wt == 0) MLA_TRACE(p, TR_EPI_END, ti.k);
           mbar_arrive(&bar[B_OFREE]);
         }
         return true;
@@ -813,6 +862,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   // ------------------------------------------------ wind down
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0) MLA_TRACE(p, TR_END, rank);
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();

@@ -39,6 +39,10 @@ std::mutex g_mutex;
 DeviceInfo g_dev[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
+#ifdef MLA_DECODE_TRACE
+unsigned long long* g_decode_trace = nullptr;  // diagnostic build only: timeline buffer
+#endif
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Per-device set-up: kernel attributes, decode cluster occupancy, status symbol.
@@ -105,9 +109,9 @@ bool encode_tiled(CUtensorMap* map, const void* base, cuuint32_t rank, const cuu
 }
 
 // Tensor maps of the decode kernel: the score CTA reads 128-row boxes of c
-// and q_cat (four 64-column blocks) and of k^R and q^R, the value CTA 64-row
-// boxes of c (all eight blocks); a block is 64 columns = 128 bytes, one
-// 128-byte-swizzle atom.
+// and q_cat (two 64-column blocks, 32 KB) and of k^R and q^R, the value CTA
+// 64-row boxes of c (all eight blocks, 64 KB); a block is 64 columns = 128
+// bytes, one 128-byte-swizzle atom.
 struct DecodeMaps {
   CUtensorMap c0, kr, q, qr, c1;
 };
@@ -120,7 +124,8 @@ bool encode_decode_maps(DecodeMaps* m, const void* q_cat, const void* c_kv, cons
                         int B, int S, int H, int Lmax) {
   const cuuint64_t rows = (cuuint64_t)B * Lmax, qrows = (cuuint64_t)B * S * H;
   const cuuint64_t c3d[3] = {64, rows, 8}, c3s[2] = {1024, 128};
-  const cuuint32_t c0b[3] = {64, (cuuint32_t)mla::kTok, 4}, c1b[3] = {64, (cuuint32_t)mla::kSub, 8};
+  const cuuint32_t c0b[3] = {64, (cuuint32_t)mla::kTok, (cuuint32_t)(mla::kCStage / mla::kBlk0)};
+  const cuuint32_t c1b[3] = {64, (cuuint32_t)mla::kSub, 8};
   const cuuint64_t kd[2] = {64, rows}, ks[1] = {128};
   const cuuint32_t b2[2] = {64, (cuuint32_t)mla::kTok};
   const cuuint64_t q3d[3] = {64, qrows, 9}, q3s[2] = {1152, 128};
@@ -218,6 +223,14 @@ const char* mla_status_string(int s) {
 }
 
 int mla_version(void) { return 100; }
+
+#ifdef MLA_DECODE_TRACE
+// Diagnostic build only: device buffer of 8-byte stamps,
+// [clusters][kTraceEvents][kTraceSlots], filled by later mla_decode calls.
+void mla_debug_set_decode_trace(void* device_buffer) {
+  g_decode_trace = static_cast<unsigned long long*>(device_buffer);
+}
+#endif
 
 }  // extern "C"
 
@@ -418,6 +431,11 @@ mla_status mla_decode(const mla_bf16* q_cat, const mla_bf16* c_kv, const mla_bf1
   p.G = w.G;
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
   p.timeout_ns = kTimeoutNs;
+#ifdef MLA_DECODE_TRACE
+  p.trace = g_decode_trace;
+#else
+  p.trace = nullptr;
+#endif
 
   return launch_ex(mla::decode_kernel, dim3(2 * w.G * w.n_rb), dim3(mla::kDecThreads), mla::kDecSmem,
                    st, true, 2, maps.c0, maps.kr, maps.q, maps.qr, maps.c1, p);
@@ -689,6 +707,7 @@ extern "C" mla_status mla_decode_noalloc(const mla_bf16* q_cat, const mla_bf16* 
   p.G = w.G;
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
   p.timeout_ns = kTimeoutNs;
+  p.trace = nullptr;
 
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
