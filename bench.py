@@ -3,14 +3,19 @@
 split-KV combine -> up-projection) on B300.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                  [--impl ours|reference] [--quick]
+                  [--impl ours|reference] [--quick] [--rope plain|yarn]
 
-Prints ONE JSON line (rank 0).  ``value`` is device time per step (us, lower
-is better) with all inputs resident in HBM and L2 flushed between steps;
-``e2e`` is the same step through the C ABI from pinned host buffers (query in,
-output back) per step.  ``--impl reference`` times the fp64 CPU oracle on a
-bounded sample of the same workload instead.  Under torchrun every rank runs
-an independent replica (no collective on the data path).
+Prints ONE JSON line (rank 0).  By default all five workloads are measured in
+one process; the headline (``value``, ``roofline``, ``e2e``, ``append``,
+``cpu_baseline``) is the largest single-GPU one, 64 sequences of U[1, 32768]
+tokens, and ``per_workload`` holds every workload's step and decode times and
+roofline fractions.  ``value`` is device time per step (us, lower is better)
+with all inputs resident in HBM and L2 flushed between steps; ``e2e`` is the
+same step through the C ABI from pinned host memory (one copy of the packed
+query inputs in, one copy of the output back) per step.  ``--workload`` limits
+the run to one workload.  ``--impl reference`` times the fp64 CPU oracle on a
+bounded sample of the headline workload instead.  Under torchrun every rank
+runs an independent replica (no collective on the data path).
 """
 from __future__ import annotations
 
@@ -33,7 +38,11 @@ sys.path.insert(0, ROOT)
 from mla_latent_kv_68_b300.inputs import WORKLOADS, bf16_bits, workload_inputs  # noqa: E402
 
 METRIC = "MLA decode µs/step, cache GB/s and TFLOP/s as fraction of B300 roofline"
-DEFAULT_WORKLOAD = "uniform_b32_s1_h128_l4096"
+# The headline is the largest workload that fits one GPU: 64 sequences of
+# U[1, 32768] cached tokens (about 1.2 GB of latent cache).
+HEADLINE = "varlen_b64_s1_h128_l1to32768"
+NOMINAL_HBM_GBS = 8000.0        # the part's nominal HBM3e bandwidth, reported beside the measured peak
+NOMINAL_BF16_TFLOPS = 2250.0    # nominal dense bf16
 CACHE_BYTES_PER_TOKEN = (512 + 64) * 2
 FLOPS_PER_VISIBLE_TOKEN_PER_HEAD = 2 * 576 + 2 * 512
 L2_FLUSH_BYTES = 256 << 20
@@ -48,9 +57,10 @@ def _peaks():
         return 6400.0, 1800.0, 1400.0, "fallback"
 
 
-def _decode_traffic():
-    """DRAM bytes per decode launch from the committed ncu summary, if the
-    decode kernel's sources are the ones that were profiled (else None)."""
+def _decode_traffic(name):
+    """DRAM bytes per decode launch of workload `name` from the committed ncu
+    summary, if the decode kernel's sources are the ones that were profiled
+    (else None)."""
     import hashlib
     import re
     h = hashlib.sha256()
@@ -59,7 +69,7 @@ def _decode_traffic():
             h.update(fh.read())
     key = h.hexdigest()[:16]
     try:
-        with open(os.path.join(ROOT, "profiles", "decode_kernel_uniform_b32_s1_h128_l4096.md")) as f:
+        with open(os.path.join(ROOT, "profiles", f"decode_kernel_{name}.md")) as f:
             m = re.search(r"traffic-key: ([0-9a-f]+) bytes: (\d+)", f.read())
     except OSError:
         return None
@@ -172,9 +182,11 @@ def _oracle_sample(x, seconds: float, seed: int = 0, rope: str = "plain"):
                          f"scaled by visible-token share {frac:.4f}")
 
 
-def run_reference(args, x, rank, world):
+def run_reference(args, rank, world):
     if rank != 0:
         return
+    name = args.workload or HEADLINE
+    x = workload_inputs(name)
     per_step = []
     for i in range(args.warmup + args.steps):
         us, threads, sample = _oracle_sample(x, seconds=args.ref_seconds, seed=i, rope=args.rope)
@@ -186,7 +198,7 @@ def run_reference(args, x, rank, world):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(v / 1000, 3), "higher_is_better": False, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": _config(args, x),
+        "config": _config(args, name, x),
         "cpu_baseline": {"value": round(v, 3), "unit": "us/step", "cores": threads,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(v, 3), "unit": "us/step", "h2d_bytes_per_step": 0,
@@ -195,9 +207,9 @@ def run_reference(args, x, rank, world):
     print(json.dumps(line), flush=True)
 
 
-def _config(args, x):
-    w = WORKLOADS[args.workload]
-    return {"workload": args.workload, "B": w.B, "S": w.S, "H": w.H,
+def _config(args, name, x):
+    w = WORKLOADS[name]
+    return {"workload": name, "B": w.B, "S": w.S, "H": w.H,
             "L": w.L if w.L is not None else f"U[{w.L_range[0]},{w.L_range[1]}]",
             "sum_L": int(x["seqlens"].sum()), "d_c": 512, "d_rope": 64,
             "l2": "flushed between timed steps (256 MiB write, then 256 MiB read)",
@@ -241,35 +253,56 @@ def _time_append(args, x, d, dev, stream, flush_l2, theta, mb):
             "launches": 2}
 
 
-def run_ours(args, x, rank, world, local_rank):
-    from mla_latent_kv_68_b300 import binding as mb
+class Packed:
+    """One pinned host buffer and one device buffer holding a step's inputs
+    (q_nope, q_rope, seqlens) back to back, 256-byte aligned, so that the
+    end-to-end step moves its inputs with a single host-to-device copy.  The
+    device views are the tensors the step (and its graphs) read."""
 
-    dev = torch.device("cuda", local_rank)
-    torch.cuda.set_device(dev)
-    mb.lib()
-    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    def __init__(self, x, dev):
+        parts = [("q_nope", x["q_nope"]), ("q_rope", x["q_rope"]), ("seqlens", x["seqlens"])]
+        offs, off = [], 0
+        for _, t in parts:
+            offs.append(off)
+            off = (off + t.numel() * t.element_size() + 255) // 256 * 256
+        self.nbytes = off
+        self.host = torch.empty(off, dtype=torch.uint8).pin_memory()
+        self.dev = torch.empty(off, dtype=torch.uint8, device=dev)
+        self.views = {}
+        for (name, t), o in zip(parts, offs):
+            n = t.numel() * t.element_size()
+            self.host[o:o + n].view(t.dtype).view(t.shape).copy_(t)
+            self.views[name] = self.dev[o:o + n].view(t.dtype).view(t.shape)
+        self.dev.copy_(self.host)
+
+
+def _roofline(wk, dec_us, hbm, tf_burst):
+    """Roofline of the decode kernel: the slower of its algorithmic bytes at
+    measured HBM bandwidth and its flops at the measured bf16 burst peak."""
+    t_hbm = wk["dec_bytes"] / (hbm * 1e3)          # us
+    t_tc = wk["dec_flops"] / (tf_burst * 1e6)      # us
+    bound = "hbm" if t_hbm >= t_tc else "tensor"
+    return bound, max(t_hbm, t_tc)
+
+
+def measure_workload(name, args, world, dev, stream, flush_l2, mb, headline=False):
+    """Time one workload's step (and its three phases) as K graph replays after
+    an L2 flush each; for the headline also the end-to-end step, the cache
+    append and the CPU oracle."""
+    x = workload_inputs(name)
     theta = mb.yarn_frequencies() if args.rope == "yarn" else None
     scale = mb.yarn_softmax_scale() if args.rope == "yarn" else mb.SOFTMAX_SCALE
+    pk = Packed(x, dev)
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v)
+         for k, v in x.items() if k not in ("q_nope", "q_rope", "seqlens")}
+    d.update(pk.views)
     mb.rope_cache(d["k_r"], d["seqlens"], theta=theta)  # cache fill: keys rotated once (untimed)
     step = mb.DecodeStep(x["B"], x["S"], x["H"], device=dev, rope_theta=theta, softmax_scale=scale)
-    stream = torch.cuda.current_stream(dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    flush_read = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-    flush_sink = torch.empty(1, dtype=torch.float32, device=dev)
-
-    def flush_l2():
-        """Write a buffer twice the size of L2, then read another one, so that
-        no line of the inputs stays cached and no dirty line of the flush is
-        left to be written back inside the timed step."""
-        flush.zero_()
-        torch.sum(flush_read.view(1, -1), dim=1, out=flush_sink)
     args_step = (d["q_nope"], d["q_rope"], d["c_kv"], d["k_r"], d["seqlens"], d["W_UK"], d["W_UV"])
-
     for _ in range(args.warmup):
         step(*args_step)
     if mb.read_status(step.workspace) != mb.MLA_OK:
-        raise RuntimeError("device status not clean after warm-up")
-
+        raise RuntimeError(f"{name}: device status not clean after warm-up")
     # CUDA graphs of the library calls: the whole step, and its three phases
     g_all = step.capture(step, *args_step)
     g_q = step.capture(step.queries, d["q_nope"], d["q_rope"], d["seqlens"], d["W_UK"])
@@ -290,82 +323,127 @@ def run_ours(args, x, rank, world, local_rank):
         _barrier(world)
         return ev
 
-    with ClockSampler(local_rank) as clocks:
-        ev_all = timed(lambda e: (e[0].record(stream), g_all.replay(), e[1].record(stream)), 2)
-        ev_ph = timed(lambda e: (e[0].record(stream), g_q.replay(), e[1].record(stream),
-                                 g_a.replay(), e[2].record(stream), g_p.replay(),
-                                 e[3].record(stream)), 4)
+    def mean_us(ev, a, b):
+        return _max_over_ranks(statistics.mean(e[a].elapsed_time(e[b]) for e in ev) * 1000, world)
+
+    ev_all = timed(lambda e: (e[0].record(stream), g_all.replay(), e[1].record(stream)), 2)
+    ev_ph = timed(lambda e: (e[0].record(stream), g_q.replay(), e[1].record(stream),
+                             g_a.replay(), e[2].record(stream), g_p.replay(),
+                             e[3].record(stream)), 4)
     if mb.read_status(step.workspace) != mb.MLA_OK:
-        raise RuntimeError("device status not clean after the timed steps")
-    step_us = _max_over_ranks(statistics.mean(e[0].elapsed_time(e[1]) for e in ev_all) * 1000, world)
-    q_us = _max_over_ranks(statistics.mean(e[0].elapsed_time(e[1]) for e in ev_ph) * 1000, world)
-    dec_us = _max_over_ranks(statistics.mean(e[1].elapsed_time(e[2]) for e in ev_ph) * 1000, world)
-    p_us = _max_over_ranks(statistics.mean(e[2].elapsed_time(e[3]) for e in ev_ph) * 1000, world)
+        raise RuntimeError(f"{name}: device status not clean after the timed steps")
+    r = {"x": x, "step_us": mean_us(ev_all, 0, 1), "q_us": mean_us(ev_ph, 0, 1),
+         "dec_us": mean_us(ev_ph, 1, 2), "p_us": mean_us(ev_ph, 2, 3)}
+    if headline:
+        # end to end through the public API from pinned host memory: one copy
+        # of the packed inputs in, the step's graph, one copy of the output back
+        hout = torch.empty(step.out.shape, dtype=torch.bfloat16).pin_memory()
 
-    # end to end through the public API from pinned host buffers: the query is
-    # copied in, the step's graph replays, the output is copied back
-    hq = x["q_nope"].pin_memory()
-    hr = x["q_rope"].pin_memory()
-    hl = x["seqlens"].pin_memory()
-    hout = torch.empty(step.out.shape, dtype=torch.bfloat16).pin_memory()
-    h2d = hq.numel() * 2 + hr.numel() * 2 + hl.numel() * 4
-    d2h = hout.numel() * 2
+        def e2e_body(e, replay=True):
+            e[0].record(stream)
+            pk.dev.copy_(pk.host, non_blocking=True)
+            if replay:
+                g_all.replay()
+            else:
+                step(*args_step)
+            hout.copy_(step.out, non_blocking=True)
+            e[1].record(stream)
 
-    def e2e_body(e, replay=True):
-        e[0].record(stream)
-        d["q_nope"].copy_(hq, non_blocking=True)
-        d["q_rope"].copy_(hr, non_blocking=True)
-        d["seqlens"].copy_(hl, non_blocking=True)
-        if replay:
-            g_all.replay()
-        else:
-            step(*args_step)
-        hout.copy_(step.out, non_blocking=True)
-        e[1].record(stream)
+        r["e2e_us"] = mean_us(timed(e2e_body, 2), 0, 1)
+        r["eager_us"] = mean_us(timed(lambda e: e2e_body(e, replay=False), 2), 0, 1)
+        r["h2d"], r["d2h"] = pk.nbytes, hout.numel() * 2
+        r["append"] = _time_append(args, x, d, dev, stream, flush_l2, theta, mb)
+    del g_all, g_q, g_a, g_p, step, d, pk
+    torch.cuda.empty_cache()
+    return r
 
-    ev_e2e = timed(e2e_body, 2)
-    e2e_us = _max_over_ranks(statistics.mean(e[0].elapsed_time(e[1]) for e in ev_e2e) * 1000, world)
-    ev_eager = timed(lambda e: e2e_body(e, replay=False), 2)
-    eager_us = _max_over_ranks(statistics.mean(e[0].elapsed_time(e[1]) for e in ev_eager) * 1000, world)
 
-    app = _time_append(args, x, d, dev, stream, flush_l2, theta, mb)
+def run_ours(args, rank, world, local_rank):
+    from mla_latent_kv_68_b300 import binding as mb
 
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    mb.lib()
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_read = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush_sink = torch.empty(1, dtype=torch.float32, device=dev)
+
+    def flush_l2():
+        """Write a buffer twice the size of L2, then read another one, so that
+        no line of the inputs stays cached and no dirty line of the flush is
+        left to be written back inside the timed step."""
+        flush.zero_()
+        torch.sum(flush_read.view(1, -1), dim=1, out=flush_sink)
+
+    names = [args.workload] if args.workload else [HEADLINE] + [n for n in WORKLOADS if n != HEADLINE]
+    head = names[0]
+    res = {}
+    with ClockSampler(local_rank) as clocks:
+        for n in names:
+            res[n] = measure_workload(n, args, world, dev, stream, flush_l2, mb, headline=(n == head))
     if rank != 0:
         return
     hbm, tf_burst, tf_sust, src = _peaks()
-    wk = _work(x)
-    achieved = wk["dec_bytes"] / (dec_us * 1e-6) / 1e9
+    per = {}
+    for n in names:
+        r = res[n]
+        wk = _work(r["x"])
+        bound, t_roof = _roofline(wk, r["dec_us"], hbm, tf_burst)
+        t_step_roof = max(wk["step_bytes"] / (hbm * 1e3), wk["step_flops"] / (tf_burst * 1e6))
+        per[n] = {"step_us": round(r["step_us"], 3), "queries_us": round(r["q_us"], 3),
+                  "decode_us": round(r["dec_us"], 3), "combine_project_us": round(r["p_us"], 3),
+                  "decode_bound": bound, "decode_roofline_us": round(t_roof, 3),
+                  "decode_frac": round(t_roof / r["dec_us"], 4),
+                  "decode_hbm_gbs": round(wk["dec_bytes"] / (r["dec_us"] * 1e-6) / 1e9, 1),
+                  "decode_tflops": round(wk["dec_flops"] / (r["dec_us"] * 1e-6) / 1e12, 1),
+                  "step_roofline_us": round(t_step_roof, 3),
+                  "step_frac": round(t_step_roof / r["step_us"], 4)}
+    r = res[head]
+    wk = _work(r["x"])
+    bound, t_roof = _roofline(wk, r["dec_us"], hbm, tf_burst)
+    if bound == "hbm":
+        achieved = wk["dec_bytes"] / (r["dec_us"] * 1e-6) / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(achieved / hbm, 4),
+                "frac_vs_nominal": round(achieved / NOMINAL_HBM_GBS, 4), "nominal_peak": NOMINAL_HBM_GBS}
+    else:
+        achieved = wk["dec_flops"] / (r["dec_us"] * 1e-6) / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": tf_burst, "unit": "TFLOP/s",
+                "frac": round(achieved / tf_burst, 4),
+                "frac_vs_nominal": round(achieved / NOMINAL_BF16_TFLOPS, 4),
+                "nominal_peak": NOMINAL_BF16_TFLOPS}
+    roof.update({"kernel": "mla_decode (the decode kernel, which plans its own split)",
+                 "traffic": _decode_traffic(head), "peak_source": src,
+                 "algorithmic_bytes": wk["dec_bytes"], "algorithmic_flops": wk["dec_flops"],
+                 "launch_us": round(r["dec_us"], 3)})
+    app = r["append"]
     line = {
-        "metric": METRIC, "value": round(step_us, 3), "unit": "us/step", "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_us / 1000, 5),
+        "metric": METRIC, "value": round(r["step_us"], 3), "unit": "us/step", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(r["step_us"] / 1000, 5),
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded; random-init weights of the pages' MLA dimensions)",
-        "config": _config(args, x),
-        "roofline": {"kernel": "mla_decode (the decode kernel, which plans its own split)", "bound": "hbm",
-                     "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-                     "frac": round(achieved / hbm, 4),
-                     "traffic": _decode_traffic() if args.workload == DEFAULT_WORKLOAD else None,
-                     "peak_source": src,
-                     "tensor_tflops": round(wk["dec_flops"] / (dec_us * 1e-6) / 1e12, 1),
-                     "tensor_frac_of_burst": round(wk["dec_flops"] / (dec_us * 1e-6) / 1e12 / tf_burst, 4)},
-        "kernels": {"queries_us": round(q_us, 3), "decode_us": round(dec_us, 3),
-                    "combine_project_us": round(p_us, 3), "step_us": round(step_us, 3),
-                    "step_roofline_us": round(max(wk["step_bytes"] / (hbm * 1e3),
-                                                  wk["step_flops"] / (tf_burst * 1e6)), 3),
+        "config": _config(args, head, r["x"]),
+        "roofline": roof,
+        "kernels": {"queries_us": round(r["q_us"], 3), "decode_us": round(r["dec_us"], 3),
+                    "combine_project_us": round(r["p_us"], 3), "step_us": round(r["step_us"], 3),
+                    "step_roofline_us": per[head]["step_roofline_us"],
                     "algorithmic_decode_bytes": wk["dec_bytes"],
                     "algorithmic_decode_flops": wk["dec_flops"]},
-        "e2e": {"value": round(e2e_us, 3), "unit": "us/step", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "path": "pinned host -> H2D -> step graph -> D2H",
-                "eager_calls_value": round(eager_us, 3)},
+        "per_workload": per,
+        "e2e": {"value": round(r["e2e_us"], 3), "unit": "us/step", "h2d_bytes_per_step": r["h2d"],
+                "d2h_bytes_per_step": r["d2h"],
+                "path": "pinned host -> one H2D copy of the packed inputs -> step graph -> one D2H copy",
+                "eager_calls_value": round(r["eager_us"], 3)},
         "append": {**app, "achieved_gbs": round(app["bytes"] / (app["us"] * 1e-6) / 1e9, 1),
                    "frac": round(app["bytes"] / (app["us"] * 1e-6) / 1e9 / hbm, 4)},
         "gpu_launches": mb.DecodeStep.LAUNCHES_PER_STEP * args.steps,
         "clocks": clocks.summary(),
     }
     if not args.quick and world == 1:
-        us, threads, sample = _oracle_sample(x, seconds=args.ref_seconds, rope=args.rope)
+        us, threads, sample = _oracle_sample(r["x"], seconds=args.ref_seconds, rope=args.rope)
         line["cpu_baseline"] = {"value": round(us, 1), "unit": "us/step", "cores": threads,
-                                "kind": "oracle", "sample": sample}
+                                "kind": "oracle", "sample": sample, "workload": head}
     print(json.dumps(line), flush=True)
 
 
@@ -388,7 +466,8 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(WORKLOADS))
+    ap.add_argument("--workload", default=None, choices=list(WORKLOADS),
+                    help="measure only this workload (default: all five, headline first)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--quick", action="store_true", help="skip the CPU-baseline timing")
     ap.add_argument("--ref-seconds", type=float, default=12.0)
@@ -409,11 +488,10 @@ def main(argv=None):
             if backend == "nccl":
                 torch.cuda.set_device(local_rank)
             torch.distributed.init_process_group(backend)
-    x = workload_inputs(args.workload)
     if args.impl == "reference":
-        run_reference(args, x, rank, world)
+        run_reference(args, rank, world)
     else:
-        run_ours(args, x, rank, world, local_rank)
+        run_ours(args, rank, world, local_rank)
     if world > 1 and args.impl == "ours":
         torch.distributed.destroy_process_group()
     return 0

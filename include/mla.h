@@ -260,6 +260,18 @@ mla_status mla_cache_append(const mla_bf16 *h, const mla_bf16 *W_DKV, const mla_
                             void *stream);
 
 /*
+ * Test hook for the kernels' bounded waits.  The next mla_decode call (only
+ * that one) launches with its split-plan barrier left incomplete: every warp
+ * that waits on it gives up after wait_limit_ns nanoseconds (instead of the
+ * usual 1 s), records MLA_ERR_TIMEOUT in the decode workspace and winds down
+ * before issuing any copy or MMA; the call writes no partial result.  Later
+ * calls are normal.  Returns MLA_ERR_INVALID_ARG unless 0 < wait_limit_ns <= 1e9.
+ * The paper has no counterpart: it exists so that a test can show that a
+ * wait that runs out is reported and leaves the device usable.
+ */
+mla_status mla_debug_decode_stall(uint64_t wait_limit_ns);
+
+/*
  * Synchronise `stream`, return the device-side status recorded in
  * `workspace` by earlier mla_decode calls (MLA_OK, MLA_ERR_BAD_SEQLEN or
  * MLA_ERR_TIMEOUT; MLA_ERR_CUDA if the stream reports an error) and clear it.

@@ -71,12 +71,13 @@ def lib():
         L.mla_cache_append_workspace_size.argtypes = [i32, i32, i32]
         L.mla_cache_append.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, sz, vp]
         L.mla_read_status.argtypes = [vp, vp]
+        L.mla_debug_decode_stall.argtypes = [ctypes.c_uint64]
         L.mla_decode_noalloc.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, f32, vp, vp]
         for n in ("mla_absorb_q", "mla_absorb_rope_q", "mla_absorb_rope_q_freq", "mla_rope_apply",
                   "mla_rope_apply_freq", "mla_rope_yarn_frequencies", "mla_rope_yarn_softmax_scale",
                   "mla_decode",
                   "mla_splitkv_combine", "mla_up_project", "mla_combine_up_project", "mla_read_status",
-                  "mla_cache_append",
+                  "mla_cache_append", "mla_debug_decode_stall",
                   "mla_decode_noalloc"):
             getattr(L, n).restype = i32
         _lib = L
@@ -301,6 +302,13 @@ def decode_noalloc(q_cat, c_kv, k_r, seqlens, o_lat, softmax_scale=SOFTMAX_SCALE
     _check(lib().mla_decode_noalloc(_ptr(q_cat), _ptr(c_kv), _ptr(k_r), _ptr(seqlens), B, S, H,
                                     Lmax, softmax_scale, _ptr(o_lat), _stream(stream)),
            "mla_decode_noalloc")
+
+
+def debug_decode_stall(wait_limit_ns: int):
+    """Test hook: the next decode() call's plan barrier is never completed, so
+    its bounded waits run out after wait_limit_ns and it reports
+    MLA_ERR_TIMEOUT (see mla_debug_decode_stall)."""
+    _check(lib().mla_debug_decode_stall(int(wait_limit_ns)), "mla_debug_decode_stall")
 
 
 def read_status(workspace=None, stream=None) -> int:

@@ -38,7 +38,8 @@ struct CombineUpParams {
   const int32_t* gfirst;
   const int32_t* segbase;
   const float2* ml;       // [slots * n_rb, 128]
-  const uint4* opart;     // [slots * n_rb][64 column octets][128 rows] fp16 x 8
+  const uint4* opart;     // [slots * n_rb][64 column octets][128 rows] fp16 x 8 (2^-e U)
+  const uint8_t* oexp;    // [slots * n_rb][128 rows][2 halves] e
   const uint32_t* plan_ok;
   __nv_bfloat16* out;     // [BS, H, 128]
   int B, S, H, n_rb, G, BS, n_tile;  // n_tile: multiple of 16, <= kCUTile
@@ -141,12 +142,16 @@ __global__ void __launch_bounds__(kCUTile * 32, 1)
                    : make_float2(0.f, 0.f);
       }
       uint4 x[2][2];
+      uint32_t ex2[2];  // the two half-row exponents of a segment (octets 0..31, 32..63)
+      const uint16_t* erow = reinterpret_cast<const uint16_t*>(p.oexp) + (size_t)rb * 128 + r;
 #pragma unroll
-      for (int j = 0; j < 2; ++j)
+      for (int j = 0; j < 2; ++j) {
 #pragma unroll
         for (int o = 0; o < 2; ++o)
           x[j][o] = j < ns ? __ldg(urow + (size_t)(k0 + j) * kstride + (size_t)(lane + 32 * o) * 128)
                            : make_uint4(0u, 0u, 0u, 0u);
+        ex2[j] = j < ns ? (uint32_t)__ldg(erow + (size_t)(k0 + j) * p.n_rb * 128) : 0u;
+      }
       float M = -INFINITY;
 #pragma unroll
       for (int u = 0; u < kCUSegLanes; ++u)
@@ -172,21 +177,24 @@ __global__ void __launch_bounds__(kCUTile * 32, 1)
         const float wj = weight(j);
         if (j < ns && wj != 0.f)  // empty groups' slots hold arbitrary bytes
 #pragma unroll
-          for (int o = 0; o < 2; ++o) acc_f16x8(acc[o], x[j][o], wj);
+          for (int o = 0; o < 2; ++o) acc_f16x8(acc[o], x[j][o], wj * pow2i((int)((ex2[j] >> (8 * o)) & 0xFFu)));
       }
       for (int j = 2; j < ns; j += 2) {  // further segments, two at a time
 #pragma unroll
-        for (int jj = 0; jj < 2; ++jj)
+        for (int jj = 0; jj < 2; ++jj) {
 #pragma unroll
           for (int o = 0; o < 2; ++o)
             x[jj][o] = j + jj < ns ? __ldg(urow + (size_t)(k0 + j + jj) * kstride + (size_t)(lane + 32 * o) * 128)
                                    : make_uint4(0u, 0u, 0u, 0u);
+          ex2[jj] = j + jj < ns ? (uint32_t)__ldg(erow + (size_t)(k0 + j + jj) * p.n_rb * 128) : 0u;
+        }
 #pragma unroll
         for (int jj = 0; jj < 2; ++jj) {
           const float wj = weight(j + jj);
           if (j + jj < ns && wj != 0.f)
 #pragma unroll
-            for (int o = 0; o < 2; ++o) acc_f16x8(acc[o], x[jj][o], wj);
+            for (int o = 0; o < 2; ++o)
+              acc_f16x8(acc[o], x[jj][o], wj * pow2i((int)((ex2[jj] >> (8 * o)) & 0xFFu)));
         }
       }
     }

@@ -90,8 +90,8 @@ constexpr int kRStage = kBlk0;             // k^R ring stage: one block (16 KB)
 constexpr int kRStages = 2;
 constexpr int kOffR = kCStages * kCStage;  // k^R ring
 constexpr int kOffQR = kOffR + kRStages * kRStage;  // q^R of the segment: 128 x 64 bf16 (A of the RoPE MMAs)
-constexpr int kOffXch = kOffQR + kBlk0;    // ceil(row max) int16 [2 tiles][2 halves][128], row sum f32 [128]
-constexpr int kXchBytes = 2 * 2 * 128 * 2 + 128 * 4;
+constexpr int kOffXch = kOffQR + kBlk0;    // ceil(row max) f32 [2 tiles][2 halves][128], row sum f32 [128]
+constexpr int kXchBytes = 2 * 2 * 128 * 4 + 128 * 4;
 // a P slot of the value CTA: P (128 x 128 bf16), rescale exponents u32 [128], row sums f32 [128]
 constexpr int kPBytes = 128 * kTok * 2;
 constexpr int kOffPEx = kPBytes;
@@ -145,12 +145,14 @@ struct DecodeParams {
   int32_t* gfirst;             // [B]
   int32_t* segbase;            // [B + 1]
   float2* ml;                  // [slots * n_rb, 128]        (m, l) per row
-  uint4* opart;                // [slots * n_rb][64 column octets][128 rows] fp16 x 8: O / l per segment
+  uint4* opart;                // [slots * n_rb][64 column octets][128 rows] fp16 x 8: 2^-e O / l per segment
+  uint8_t* oexp;               // [slots * n_rb][128 rows][2 column halves]: the exponent e of each half row
   uint32_t* status;
   uint32_t* plan_ok;           // written by CTA 0
   int B, S, H, Lmax, n_rb, G;
   float scale_log2;            // softmax_scale * log2(e)
   uint64_t timeout_ns;
+  uint32_t plan_arrivals;      // arrivals that complete the plan barrier: 1 (2 for the stall test hook)
   unsigned long long* trace;   // timeline of a diagnostic build (MLA_DECODE_TRACE), else unused
 };
 
@@ -398,6 +400,51 @@ __device__ __forceinline__ float exp2_int(int d) {
   return d <= -127 ? 0.f : __int_as_float((127 + d) << 23);
 }
 
+// Value CTA, end of a segment: the thread's half row of O (256 columns at
+// tensor-memory address `ta`) leaves as 2^-e O / l in fp16, stored as
+// [64 column octets][128 rows] of 16 bytes, so that each store of a warp
+// covers 32 consecutive rows, 512 contiguous bytes (the epilogue is bound by
+// an SM's store bandwidth, so halving the bytes against fp32 O halves its
+// time).  O / l is a convex mix of cache rows; e >= 0 (stored beside, one per
+// half row) is 0 unless some |O / l| reaches 2^15, and then the smallest
+// power of two that brings every value of the half row below 2^15, so no
+// cache value, however large, overflows fp16.  Kept out of line: it runs
+// once per segment, and the per-tile loop around it stays small.
+__device__ __noinline__ void store_partial(const DecodeParams& p, uint32_t ta, int hf, int r, int rb, int slot,
+                                           float l_seg, bool valid) {
+  const float inv0 = l_seg > 0.f ? 1.f / l_seg : 0.f;
+  uint4* dst = p.opart + ((size_t)slot * p.n_rb + rb) * 64 * 128 + r;
+  float amax = 0.f;
+  int e = 0;
+  for (int pass = 0; pass < 2; ++pass) {  // a second pass only when the first went out of range
+    const float inv = inv0 * exp2_int(-e);
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+      uint32_t v[64];
+      {
+        uint32_t (&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[0]);
+        uint32_t (&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[32]);
+        tmem_ld32(ta + (uint32_t)(c * 64), lo);
+        tmem_ld32(ta + (uint32_t)(c * 64 + 32), hi);
+      }
+      tmem_wait_ld();
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const float* f = reinterpret_cast<const float*>(&v[8 * u]);
+#pragma unroll
+        for (int t = 0; t < 8; ++t) amax = fmaxf(amax, fabsf(f[t]));
+        dst[(size_t)(hf * 32 + c * 8 + u) * 128] =
+            make_uint4(pack_f16x2_sat(f[0] * inv, f[1] * inv), pack_f16x2_sat(f[2] * inv, f[3] * inv),
+                       pack_f16x2_sat(f[4] * inv, f[5] * inv), pack_f16x2_sat(f[6] * inv, f[7] * inv));
+      }
+    }
+    const float top = amax * inv0;  // largest |O / l| of the half row
+    if (pass == 1 || !(top >= 32768.f)) break;
+    e = max(0, (int)((__float_as_uint(top) >> 23) & 0xFFu) - 141);  // top < 2^(biased exp - 126) <= 2^(15 + e)
+  }
+  if (valid) p.oexp[(((size_t)slot * p.n_rb + rb) * 128 + r) * 2 + hf] = (uint8_t)e;
+}
+
 __global__ void __launch_bounds__(kDecThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tm_c0, const __grid_constant__ CUtensorMap tm_kr,
                   const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_qr,
@@ -438,7 +485,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     mbar_init(&bar[B_DRAIN], 1);
     mbar_init(&bar[B_QRFULL], 1);
     mbar_init(&bar[B_QREMPTY], 1);
-    mbar_init(&bar[B_PLAN], 1);
+    // one arrival (the plan warp's); the stall test hook asks for two, so the
+    // barrier never completes and every wait on it runs out
+    mbar_init(&bar[B_PLAN], p.plan_arrivals);
     if (rank == 1) {  // first phase of each P slot expects one slot's bytes
       mbar_arrive_expect_tx(&bar[B_PFULL + 0], kPTx);
       mbar_arrive_expect_tx(&bar[B_PFULL + 1], kPTx);
@@ -656,8 +705,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 
     if (rank == 0) {
       // ---------------------------------------- scores + online softmax
-      int16_t* xch = reinterpret_cast<int16_t*>(smem + kOffXch);          // [2][2][128]
-      float* xl = reinterpret_cast<float*>(smem + kOffXch + 2 * 2 * 128 * 2);  // [128]
+      float* xch = reinterpret_cast<float*>(smem + kOffXch);                  // [2][2][128]
+      float* xl = reinterpret_cast<float*>(smem + kOffXch + 2 * 2 * 128 * 4);  // [128]
       // P, the rescale exponent and the row sum go straight into the value
       // CTA's P slot as asynchronous remote stores, each counted (in bytes) on
       // that slot's barrier there.
@@ -699,21 +748,20 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         // Both threads of the row (same quadrant, warps q4 and q4 + 4) need the
         // same new reference exponent, which depends on the row maximum only
         // through ceil(max): for an integer m, max > m + 8 iff ceil(max) > m + 8.
-        // So the two halves exchange ceil(max) as a 16-bit integer.
-        const int cm = mx == -INFINITY ? -32768 : (int)fminf(fmaxf(ceilf(mx), -32000.f), 32000.f);
-        xch[(slot * 2 + hf) * 128 + r] = (int16_t)cm;
+        // So the two halves exchange ceil(max) (-inf when no column is visible).
+        const float cm = ceilf(mx);
+        xch[(slot * 2 + hf) * 128 + r] = cm;
         if (!ti.dry) {
           mbar_arrive(&bar[B_XCH + slot * 4 + q4]);
           if (!warp_wait(&bar[B_XCH + slot * 4 + q4], sph, wc)) return false;
         }
         if (!ti.dry && threadIdx.x == 128) MLA_TRACE(p, TR_SM_XCH, ti.i);
-        const int cmax = max(cm, (int)xch[(slot * 2 + (hf ^ 1)) * 128 + r]);
+        const float cmax = fmaxf(cm, xch[(slot * 2 + (hf ^ 1)) * 128 + r]);
         int ex = 0;  // rescale 2^-ex of O and l; 255 stands for 0
-        if (cmax > -32768 && (float)cmax > m_ref + 8.f) {
-          const float mn = (float)cmax;
-          ex = (m_ref == -INFINITY) ? 255 : min((int)(mn - m_ref), 255);
+        if (cmax > m_ref + 8.f) {  // never for -inf; m is a float holding an integer
+          ex = (m_ref == -INFINITY) ? 255 : (int)fminf(cmax - m_ref, 255.f);
           l = (ex == 255) ? 0.f : l * exp2_int(-ex);
-          m_ref = mn;
+          m_ref = cmax;
         }
         const float mu = (m_ref == -INFINITY) ? 0.f : m_ref;
 
@@ -825,31 +873,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
           if (!warp_wait(&bar[B_PVDONE + slot], sph, wc)) return false;
           if (wt == 0) MLA_TRACE(p, TR_EPI_BEGIN, ti.k);
           tc_fence_after();
-          // O / l in fp16 as [64 column octets][128 rows] of 16 bytes: each
-          // store of a warp covers 32 consecutive rows, 512 contiguous bytes.
-          // The epilogue is bound by an SM's store bandwidth, so halving the
-          // bytes (against fp32 O) halves its time; normalising first keeps
-          // the values within fp16 range (a convex mix of cache rows).
-          const float inv = l_seg > 0.f ? 1.f / l_seg : 0.f;
-          uint4* dst = p.opart + ((size_t)ti.slot * p.n_rb + rb) * 64 * 128 + r;
-#pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
-            uint32_t v[64];
-            {
-              uint32_t (&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[0]);
-              uint32_t (&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[32]);
-              tmem_ld32(tl + (uint32_t)(hf * 256 + c * 64), lo);
-              tmem_ld32(tl + (uint32_t)(hf * 256 + c * 64 + 32), hi);
-            }
-            tmem_wait_ld();
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              const float* f = reinterpret_cast<const float*>(&v[8 * u]);
-              dst[(size_t)(hf * 32 + c * 8 + u) * 128] =
-                  make_uint4(pack_f16x2_sat(f[0] * inv, f[1] * inv), pack_f16x2_sat(f[2] * inv, f[3] * inv),
-                             pack_f16x2_sat(f[4] * inv, f[5] * inv), pack_f16x2_sat(f[6] * inv, f[7] * inv));
-            }
-          }
+          store_partial(p, tl + (uint32_t)(hf * 256), hf, r, rb, ti.slot, l_seg, valid);
           tc_fence_before();
           if (wt == 0) MLA_TRACE(p, TR_EPI_END, ti.k);
           mbar_arrive(&bar[B_OFREE]);

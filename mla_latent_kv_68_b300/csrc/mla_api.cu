@@ -8,6 +8,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include "mla.h"
@@ -42,6 +43,10 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 #ifdef MLA_DECODE_TRACE
 unsigned long long* g_decode_trace = nullptr;  // diagnostic build only: timeline buffer
 #endif
+
+// Test hook (mla_debug_decode_stall): the wait limit of the next mla_decode
+// call whose plan barrier is left incomplete; 0 = none pending.
+std::atomic<uint64_t> g_stall_ns{0};
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -138,7 +143,7 @@ bool encode_decode_maps(DecodeMaps* m, const void* q_cat, const void* c_kv, cons
 // Workspace layout of mla_decode / mla_splitkv_combine.
 struct WsLayout {
   int n_rb = 0, G = 0, slots = 0;
-  size_t prefix = 0, gfirst = 0, segbase = 0, ml = 0, opart = 0, total = 0;
+  size_t prefix = 0, gfirst = 0, segbase = 0, ml = 0, opart = 0, oexp = 0, total = 0;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -155,6 +160,7 @@ WsLayout ws_layout(int B, int S, int H, int max_clusters) {
   w.segbase = off; off = align256(off + sizeof(int32_t) * (B + 1));
   w.ml = off;      off = align256(off + sizeof(float) * 2 * (size_t)w.slots * w.n_rb * 128);
   w.opart = off;   off = align256(off + sizeof(uint16_t) * (size_t)w.slots * w.n_rb * 128 * 512);
+  w.oexp = off;    off = align256(off + (size_t)w.slots * w.n_rb * 128 * 2);
   w.total = off;
   return w;
 }
@@ -421,6 +427,7 @@ mla_status mla_decode(const mla_bf16* q_cat, const mla_bf16* c_kv, const mla_bf1
   p.segbase = reinterpret_cast<int32_t*>(ws + w.segbase);
   p.ml = reinterpret_cast<float2*>(ws + w.ml);
   p.opart = reinterpret_cast<uint4*>(ws + w.opart);
+  p.oexp = ws + w.oexp;
   p.status = reinterpret_cast<uint32_t*>(ws);
   p.plan_ok = reinterpret_cast<uint32_t*>(ws) + 1;
   p.B = B;
@@ -431,6 +438,11 @@ mla_status mla_decode(const mla_bf16* q_cat, const mla_bf16* c_kv, const mla_bf1
   p.G = w.G;
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
   p.timeout_ns = kTimeoutNs;
+  p.plan_arrivals = 1u;
+  if (const uint64_t stall = g_stall_ns.exchange(0)) {
+    p.plan_arrivals = 2u;
+    p.timeout_ns = stall;
+  }
 #ifdef MLA_DECODE_TRACE
   p.trace = g_decode_trace;
 #else
@@ -459,6 +471,7 @@ mla_status mla_splitkv_combine(const void* workspace, size_t workspace_bytes, ml
   p.segbase = reinterpret_cast<const int32_t*>(ws + w.segbase);
   p.ml = reinterpret_cast<const float2*>(ws + w.ml);
   p.opart = reinterpret_cast<const uint4*>(ws + w.opart);
+  p.oexp = ws + w.oexp;
   p.o_lat = reinterpret_cast<__nv_bfloat16*>(o_lat);
   p.plan_ok = reinterpret_cast<const uint32_t*>(ws) + 1;
   p.B = B;
@@ -532,6 +545,7 @@ mla_status mla_combine_up_project(const void* workspace, size_t workspace_bytes,
   p.segbase = reinterpret_cast<const int32_t*>(ws + w.segbase);
   p.ml = reinterpret_cast<const float2*>(ws + w.ml);
   p.opart = reinterpret_cast<const uint4*>(ws + w.opart);
+  p.oexp = ws + w.oexp;
   p.plan_ok = reinterpret_cast<const uint32_t*>(ws) + 1;
   p.out = reinterpret_cast<__nv_bfloat16*>(out);
   p.B = B;
@@ -610,6 +624,12 @@ mla_status mla_cache_append(const mla_bf16* h, const mla_bf16* W_DKV, const mla_
   f.Lmax = Lmax;
   return launch_ex(mla::append_finalize_kernel, dim3((unsigned)BS), dim3(mla::kAppCols / 2), 0, st, true, 1,
                    f, th);
+}
+
+mla_status mla_debug_decode_stall(uint64_t wait_limit_ns) {
+  if (wait_limit_ns == 0 || wait_limit_ns > kTimeoutNs) return MLA_ERR_INVALID_ARG;
+  g_stall_ns.store(wait_limit_ns);
+  return MLA_OK;
 }
 
 mla_status mla_read_status(void* workspace, void* stream) {
@@ -697,6 +717,7 @@ extern "C" mla_status mla_decode_noalloc(const mla_bf16* q_cat, const mla_bf16* 
   p.segbase = reinterpret_cast<int32_t*>(ws + w.segbase);
   p.ml = reinterpret_cast<float2*>(ws + w.ml);
   p.opart = reinterpret_cast<uint4*>(ws + w.opart);
+  p.oexp = ws + w.oexp;
   p.status = status;
   p.plan_ok = plan_ok;
   p.B = B;
@@ -707,6 +728,7 @@ extern "C" mla_status mla_decode_noalloc(const mla_bf16* q_cat, const mla_bf16* 
   p.G = w.G;
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
   p.timeout_ns = kTimeoutNs;
+  p.plan_arrivals = 1u;
   p.trace = nullptr;
 
   cudaLaunchConfig_t cfg = {};
@@ -731,6 +753,7 @@ extern "C" mla_status mla_decode_noalloc(const mla_bf16* q_cat, const mla_bf16* 
   cp.segbase = p.segbase;
   cp.ml = p.ml;
   cp.opart = p.opart;
+  cp.oexp = p.oexp;
   cp.o_lat = reinterpret_cast<__nv_bfloat16*>(o_lat);
   cp.plan_ok = plan_ok;
   cp.B = B;

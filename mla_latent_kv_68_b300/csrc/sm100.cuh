@@ -326,6 +326,9 @@ __device__ __forceinline__ void st_async_b32(uint32_t raddr, uint32_t v, uint32_
                : "memory");
 }
 
+// Exact 2^e for an integer 0 <= e <= 127.
+__device__ __forceinline__ float pow2i(int e) { return __int_as_float((127 + e) << 23); }
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);

@@ -6,8 +6,9 @@
 // 128-row tiles ("segments") spread over all SMs; each segment k leaves, per
 // query row, its reference exponent m_k (an integer, log2 units), the sum
 // l_k = sum_j 2^(s2_j - m_k) and the normalised latent mix
-// U_k = sum_j 2^(s2_j - m_k) c_j / l_k (fp16).  Merging them restores the
-// single normalisation:
+// U_k = sum_j 2^(s2_j - m_k) c_j / l_k, stored in fp16 as 2^-e U_k with one
+// exponent e >= 0 per row and 256-column half that keeps it in fp16 range.
+// Merging them restores the single normalisation:
 //     o_lat = sum_k w_k U_k / sum_k w_k,   w_k = 2^(m_k - M) l_k,   M = max_k m_k.
 //
 // Tiles are kTileRows = 128 cache rows (the N of the decode's QK^T MMAs).
@@ -38,7 +39,8 @@ struct CombineParams {
   const int32_t* gfirst;
   const int32_t* segbase;
   const float2* ml;     // [slots * n_rb, 128] (m_k, l_k)
-  const uint4* opart;   // [slots * n_rb][64 column octets][128 rows] fp16 x 8 (U_k)
+  const uint4* opart;   // [slots * n_rb][64 column octets][128 rows] fp16 x 8 (2^-e U_k)
+  const uint8_t* oexp;  // [slots * n_rb][128 rows][2 halves] e
   __nv_bfloat16* o_lat; // [B*S*H, 512]
   const uint32_t* plan_ok;
   int B, S, H, n_rb, G;
@@ -79,8 +81,10 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
   float acc[kCombineCols];
 #pragma unroll
   for (int i = 0; i < kCombineCols; ++i) acc[i] = 0.f;
+  const int half = c0 >> 8;  // which exponent of the row applies to these columns
   for (int kb = k0; kb < k1; kb += kSegBatch) {
     float2 ml[kSegBatch];
+    int ee[kSegBatch];
     uint4 x[kSegBatch][kCombineCols / 8];
 #pragma unroll
     for (int u = 0; u < kSegBatch; ++u) {
@@ -88,6 +92,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
       const bool ok = k < k1 && !(may_be_empty && group_empty(g0 + k - k0, T, p.G));
       const size_t idx = (size_t)k * p.n_rb + rb;
       ml[u] = ok ? __ldg(&p.ml[idx * 128 + r]) : make_float2(0.f, 0.f);
+      ee[u] = ok ? (int)__ldg(&p.oexp[(idx * 128 + r) * 2 + half]) : 0;
 #pragma unroll
       for (int c = 0; c < kCombineCols / 8; ++c)
         x[u][c] = ok ? __ldg(p.opart + (idx * 64 + c0 / 8 + c) * 128 + r) : make_uint4(0u, 0u, 0u, 0u);
@@ -108,14 +113,15 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
       if (!(ml[u].y > 0.f)) continue;  // no segment, or no visible row in it
       const float w = exp2f(ml[u].x - M) * ml[u].y;
       den += w;
+      const float wu = w * pow2i(ee[u]);  // the stored partial is 2^-e U
 #pragma unroll
       for (int c = 0; c < kCombineCols / 8; ++c) {
         const uint32_t* h = reinterpret_cast<const uint32_t*>(&x[u][c]);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h[e]));
-          acc[8 * c + 2 * e] += w * f.x;
-          acc[8 * c + 2 * e + 1] += w * f.y;
+          acc[8 * c + 2 * e] += wu * f.x;
+          acc[8 * c + 2 * e + 1] += wu * f.y;
         }
       }
     }

@@ -93,3 +93,8 @@ def test_combine_up_project_host_validation(lib):
     assert lib.mla_combine_up_project(fake, 1 << 30, fake, fake, 1, 1, 200, None) == 2
     assert lib.mla_combine_up_project(fake, 1 << 30, fake, fake, 1, 17, 128, None) == 2  # S*H > 2048
     assert lib.mla_combine_up_project(nul, 1 << 30, fake, fake, 1, 1, 16, None) == 3
+
+
+def test_decode_stall_hook_rejects_bad_limits(lib):
+    assert lib.mla_debug_decode_stall(ctypes.c_uint64(0)) == 1            # MLA_ERR_INVALID_ARG
+    assert lib.mla_debug_decode_stall(ctypes.c_uint64(2_000_000_000)) == 1

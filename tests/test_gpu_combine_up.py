@@ -97,3 +97,31 @@ def test_combine_up_step_runs_twice_alike():
         outs.append(out)
     assert mb.read_status(ws) == mb.MLA_OK
     assert torch.equal(outs[0], outs[1])
+
+
+def test_combine_up_with_cache_values_beyond_fp16_range():
+    # cache rows near 1e5 (see the decode test of the same name): the split
+    # partials carry a power-of-two exponent per half row, which the fused
+    # merge applies before the up-projection
+    g = torch.Generator().manual_seed(41)
+    B, S, H, seqlens = 2, 1, 128, [7000, 2500]
+    Lmax = max(seqlens)
+    c = torch.zeros(B, Lmax, 512)
+    k = torch.zeros(B, Lmax, 64)
+    for b, L in enumerate(seqlens):
+        c[b, :L] = 1e5 * (1.0 + 0.01 * torch.randn(L, 512, generator=g))
+        k[b, :L] = torch.randn(L, 64, generator=g)
+    q = torch.cat([5e-4 * torch.randn(B, S, H, 512, generator=g),
+                   torch.randn(B, S, H, 64, generator=g)], dim=-1).to(torch.bfloat16)
+    c, k = c.to(torch.bfloat16), k.to(torch.bfloat16)
+    W = (torch.randn(H, 128, 512, generator=g) / math.sqrt(512)).to(torch.bfloat16)
+    sl = torch.tensor(seqlens, dtype=torch.int32)
+    ws = mb.new_workspace(B, S, H)
+    mb.decode(q.cuda(), c.cuda(), k.cuda(), sl.cuda(), ws)
+    fused = torch.full((B, S, H, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    mb.combine_up_project(ws, W.cuda(), fused)
+    assert mb.read_status(ws) == mb.MLA_OK
+    lat = oracle.latent_attention(bits(q), bits(c), bits(k), sl.numpy(), d_r=64, softmax_scale=SCALE)
+    ref = np.einsum("bshk,hvk->bshv", lat, W.double().numpy())
+    assert np.abs(lat).max() > 65504.0
+    assert_close(f64(fused) / 1e5, ref / 1e5, what="fused merge, cache values near 1e5")

@@ -195,6 +195,45 @@ def test_decode_ignores_nan_padding():
     assert_close(got, ref, what="nan padding")
 
 
+def test_large_cache_values_keep_the_split_partials_in_range():
+    # Cache rows near 1e5 (a common offset plus 1% noise): every latent mix
+    # U = O / l of a split is near 1e5, beyond fp16's 65504, so the stored
+    # partials need their per-half-row power-of-two exponent.  The queries are
+    # scaled down so the scores stay ordinary; compare relative to 1e5.
+    g = torch.Generator().manual_seed(31)
+    B, S, H, seqlens = 3, 1, 128, [5000, 300, 9000]
+    Lmax = max(seqlens)
+    c = torch.zeros(B, Lmax, 512)
+    k = torch.zeros(B, Lmax, 64)
+    for b, L in enumerate(seqlens):
+        c[b, :L] = 1e5 * (1.0 + 0.01 * torch.randn(L, 512, generator=g))
+        k[b, :L] = torch.randn(L, 64, generator=g)
+    q = torch.cat([5e-4 * torch.randn(B, S, H, 512, generator=g),
+                   torch.randn(B, S, H, 64, generator=g)], dim=-1)
+    q, c, k = q.to(torch.bfloat16), c.to(torch.bfloat16), k.to(torch.bfloat16)
+    sl = torch.tensor(seqlens, dtype=torch.int32)
+    got = _run_latent(q, c, k, sl)
+    ref = oracle.latent_attention(bits(q), bits(c), bits(k), sl.numpy(), d_r=64,
+                                  softmax_scale=1.0 / math.sqrt(192.0))
+    assert np.abs(ref).max() > 65504.0
+    assert_close(got / 1e5, ref / 1e5, what="cache values near 1e5")
+
+
+def test_huge_scores_select_the_top_key():
+    # Queries scaled by 1e4: scores reach tens of thousands in log2 units,
+    # far from each other, so the softmax is one-hot on each row's top key;
+    # the row maximum is carried as a float (no clamp on its range).
+    B, S, H, seqlens = 2, 2, 64, [1000, 777]
+    q, c, k, sl = _latent_case(B, S, H, seqlens, seed=33)
+    q = (q.float() * torch.cat([torch.full((512,), 1e4), torch.ones(64)])).to(torch.bfloat16)
+    got = _run_latent(q, c, k, sl)
+    ref = oracle.latent_attention(bits(q), bits(c), bits(k), sl.numpy(), d_r=64,
+                                  softmax_scale=1.0 / math.sqrt(192.0))
+    s2 = (q[..., :512].double() @ c.double().transpose(1, 2).unsqueeze(1)) / math.sqrt(192.0) / math.log(2.0)
+    assert s2.abs().max() > 32000.0
+    assert_close(got, ref, what="one-hot rows")
+
+
 def test_bad_seqlen_is_reported_and_recovers():
     q, c, k, sl = _latent_case(2, 2, 16, [5, 9], seed=11)
     ws = mb.new_workspace(2, 2, 16)

@@ -11,11 +11,13 @@ shared scratch does not leak into its result.  This file is collected last so
 that a failure here cannot hide another test's result.
 """
 import ctypes
+import math
 
 import pytest
 import torch
 
-from gpu_util import assert_close, f64
+import oracle
+from gpu_util import assert_close, bits, f64
 from mla_latent_kv_68_b300 import binding as mb
 
 pytestmark = pytest.mark.gpu
@@ -73,6 +75,10 @@ def test_noalloc_matches_regular_decode_on_two_calls_in_a_row():
         want = f64(_regular(q, c, k, sl))
         got = f64(_noalloc(q, c, k, sl))
         assert_close(got, want, what=f"noalloc vs regular B{B} S{S} H{H}")
+        # and against the fp64 oracle of the absorbed latent attention
+        ref = oracle.latent_attention(bits(q.cpu()), bits(c.cpu()), bits(k.cpu()), sl.cpu().numpy(),
+                                      d_r=64, softmax_scale=1.0 / math.sqrt(192.0))
+        assert_close(got, ref, what=f"noalloc vs oracle B{B} S{S} H{H}")
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch():
