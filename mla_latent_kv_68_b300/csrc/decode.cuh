@@ -557,15 +557,17 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             qr_last = ti.k;
             tma_load_2d(smem + kOffQR, &tm_qr, &bar[B_QRFULL], 512, qrow0);
           }
+          {  // the tile's k^R first: its MMAs open the tile's QK^T
+            const int st = slot(kBarR, kRStages, rq++, kRStage);
+            if (st < 0) return false;
+            tma_load_2d(smem + kOffR + st * kRStage, &tm_kr, &bar[B_FULL + kBarR + st], 0, row0);
+          }
           for (int h = 0; h < kCPerTile; ++h, ++cq) {
             const int st = slot(kBarC, kCStages, cq, kCStage);
             if (st < 0) return false;
             if (h == 0) MLA_TRACE(p, TR_TMA_ISSUE, ti.i);
             tma_load_3d(smem + st * kCStage, &tm_c0, &bar[B_FULL + kBarC + st], 0, row0, 4 * h);
           }
-          const int st = slot(kBarR, kRStages, rq++, kRStage);
-          if (st < 0) return false;
-          tma_load_2d(smem + kOffR + st * kRStage, &tm_kr, &bar[B_FULL + kBarR + st], 0, row0);
         } else {
           const int nsub = (ti.nvt + kSub - 1) / kSub;
           for (int u = 0; u < nsub; ++u, ++q) {  // 64-row stages of the 512 c columns
@@ -614,30 +616,31 @@ __global__ void __launch_bounds__(kDecThreads, 1)
           }
           if (!mbar_wait(&bar[B_SEMPTY + sb], sph ^ 1u, wc)) return false;
           const uint32_t d = tmem + (uint32_t)sb * 128u;
-          for (int h = 0; h < kCPerTile; ++h) {  // c blocks 2h, 2h + 1 against q~ from tensor memory
+          {  // k^R against q^R, both 64 wide and K-major in shared memory; they open S
+            const int q = ti.i, st = q % kRStages;
+            if (!mbar_wait(&bar[B_FULL + kBarR + st], (uint32_t)(q / kRStages) & 1u, wc)) return false;
+            tc_fence_after();
+            MLA_TRACE(p, TR_QK_BEGIN, ti.i);
+            const uint32_t sbase = smem_u32(smem + kOffR + st * kRStage), qbase = smem_u32(smem + kOffQR);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_ss(d, smem_desc(qbase + kk * 32, 16, 1024, 2), smem_desc(sbase + kk * 32, 16, 1024, 2), idesc,
+                     kk > 0 ? 1u : 0u);
+            mma_commit(&bar[B_EMPTY + kBarR + st]);
+          }
+          for (int h = 0; h < kCPerTile; ++h) {  // c blocks 4h .. 4h + 3 against q~ from tensor memory
             const int q = cpos_kv(ti.i, ti.k, h), st = q % kCStages;
             if (!mbar_wait(&bar[B_FULL + kBarC + st], (uint32_t)(q / kCStages) & 1u, wc)) return false;
             if (h == kCPerTile - 1) MLA_TRACE(p, TR_QK_LAST, ti.i);
             tc_fence_after();
             const uint32_t sbase = smem_u32(smem + st * kCStage);
-            if (h == 0) MLA_TRACE(p, TR_QK_BEGIN, ti.i);
 #pragma unroll
             for (int kk = 0; kk < 16; ++kk) {  // 4 blocks x 4 K-steps of 16
               const int gk = h * 16 + kk;
               const uint64_t bd = smem_desc(sbase + (kk >> 2) * kBlk0 + (kk & 3) * 32, 16, 1024, 2);
-              mma_ts(d, tmem + kQCol + (uint32_t)gk * 8, bd, idesc, gk > 0 ? 1u : 0u);
+              mma_ts(d, tmem + kQCol + (uint32_t)gk * 8, bd, idesc, 1u);
             }
             mma_commit(&bar[B_EMPTY + kBarC + st]);
-          }
-          {  // k^R against q^R, both 64 wide and K-major in shared memory
-            const int q = ti.i, st = q % kRStages;
-            if (!mbar_wait(&bar[B_FULL + kBarR + st], (uint32_t)(q / kRStages) & 1u, wc)) return false;
-            tc_fence_after();
-            const uint32_t sbase = smem_u32(smem + kOffR + st * kRStage), qbase = smem_u32(smem + kOffQR);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_ss(d, smem_desc(qbase + kk * 32, 16, 1024, 2), smem_desc(sbase + kk * 32, 16, 1024, 2), idesc, 1u);
-            mma_commit(&bar[B_EMPTY + kBarR + st]);
           }
           if (ti.last) mma_commit(&bar[B_QREMPTY]);  // the next segment may replace q~ and q^R
           mma_commit(&bar[B_SFULL + sb]);
