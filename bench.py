@@ -353,9 +353,44 @@ def measure_workload(name, args, world, dev, stream, flush_l2, mb, headline=Fals
         r["eager_us"] = mean_us(timed(lambda e: e2e_body(e, replay=False), 2), 0, 1)
         r["h2d"], r["d2h"] = pk.nbytes, hout.numel() * 2
         r["append"] = _time_append(args, x, d, dev, stream, flush_l2, theta, mb)
+        r["oproj"] = _time_output_project(args, x, dev, stream, flush_l2, mb)
     del g_all, g_q, g_a, g_p, step, d, pk
     torch.cuda.empty_cache()
     return r
+
+
+def _time_output_project(args, x, dev, stream, flush_l2, mb):
+    """The layer's output projection after the step (not part of its time):
+    u = W^O [o_1; ...; o_H] for the step's B*S tokens, W^O [7168, H*128]
+    bf16, recorded in a graph and replayed after an L2 flush."""
+    B, S, H = x["B"], x["S"], x["H"]
+    BS, K = B * S, H * 128
+    g = torch.Generator().manual_seed(68200)
+    xo = torch.randn(BS, K, generator=g).to(torch.bfloat16).to(dev)
+    W = (torch.randn(APPEND_D, K, generator=g) / K ** 0.5).to(torch.bfloat16).to(dev)
+    u = torch.empty(BS, APPEND_D, dtype=torch.bfloat16, device=dev)
+    ws = mb.output_project_workspace(BS, K, APPEND_D, device=dev)
+    for _ in range(max(3, args.warmup)):
+        mb.output_project(xo, W, u, ws)
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr):
+        mb.output_project(xo, W, u, ws)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    torch.cuda.synchronize(dev)
+    for e in ev:
+        flush_l2()
+        e[0].record(stream)
+        gr.replay()
+        e[1].record(stream)
+    torch.cuda.synchronize(dev)
+    if mb.read_status() != mb.MLA_OK:
+        raise RuntimeError("device status not clean after the output projection")
+    us = statistics.mean(e[0].elapsed_time(e[1]) for e in ev) * 1000
+    nbytes = APPEND_D * K * 2 + BS * K * 2 + BS * APPEND_D * 2
+    del W, xo, u, ws
+    torch.cuda.empty_cache()
+    return {"workload": f"{BS} tokens, W^O [{APPEND_D}, {K}]", "us": round(us, 3), "bytes": nbytes,
+            "launches": 2}
 
 
 def run_ours(args, rank, world, local_rank):
@@ -437,6 +472,9 @@ def run_ours(args, rank, world, local_rank):
                 "eager_calls_value": round(r["eager_us"], 3)},
         "append": {**app, "achieved_gbs": round(app["bytes"] / (app["us"] * 1e-6) / 1e9, 1),
                    "frac": round(app["bytes"] / (app["us"] * 1e-6) / 1e9 / hbm, 4)},
+        "output_projection": {**r["oproj"],
+                              "achieved_gbs": round(r["oproj"]["bytes"] / (r["oproj"]["us"] * 1e-6) / 1e9, 1),
+                              "frac": round(r["oproj"]["bytes"] / (r["oproj"]["us"] * 1e-6) / 1e9 / hbm, 4)},
         "gpu_launches": mb.DecodeStep.LAUNCHES_PER_STEP * args.steps,
         "clocks": clocks.summary(),
     }

@@ -260,6 +260,29 @@ mla_status mla_cache_append(const mla_bf16 *h, const mla_bf16 *W_DKV, const mla_
                             void *stream);
 
 /*
+ * The attention layer's output projection, one token at a time:
+ *     u[n] = W x[n]          (u [BS][d], W [d][K], x [BS][K], all bf16 row-major)
+ * with fp32 accumulation on the tensor cores, rounded to bf16.  "DeepSeek-V3"
+ * (ekkoxiao.github.io), "注意力计算": u_t = W^O [o_{t,1}; ...; o_{t,H}], so
+ *   x = out of mla_up_project viewed as [BS][H * 128] and W = W^O [d][H * 128];
+ * and, with the value up-projection absorbed into W^O ("DeepSeek-V3
+ * 技术报告精读" (oopvo.github.io), "MLA"),
+ *   x = o_lat viewed as [BS][H * 512] and W = W^O blockdiag(W_h^UV)
+ *   [d][H * 512], a weight the caller forms once (4x the bytes of W^O for
+ *   d_c = 512, d_v = 128, so the unfolded pair streams less per step).
+ * Requires K and d multiples of 128.  workspace: at least
+ * mla_output_project_workspace_size(BS, K, d) bytes, 256-byte aligned (may be
+ * NULL when that size is 0); it holds fp32 partial products over slices of K,
+ * summed in a fixed order by a second launch.  x is read after the kernel
+ * launched before this one finishes; W may stream in before, so it must not
+ * be written by that kernel.  Device-side errors go to the library status
+ * word (mla_read_status(NULL, stream)).
+ */
+size_t mla_output_project_workspace_size(int BS, int K, int d);
+mla_status mla_output_project(const mla_bf16 *x, const mla_bf16 *W, mla_bf16 *u, int BS, int K, int d,
+                              void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Test hook for the kernels' bounded waits.  The next mla_decode call (only
  * that one) launches with its split-plan barrier left incomplete: every warp
  * that waits on it gives up after wait_limit_ns nanoseconds (instead of the

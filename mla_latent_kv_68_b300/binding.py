@@ -72,12 +72,15 @@ def lib():
         L.mla_cache_append.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, sz, vp]
         L.mla_read_status.argtypes = [vp, vp]
         L.mla_debug_decode_stall.argtypes = [ctypes.c_uint64]
+        L.mla_output_project_workspace_size.restype = sz
+        L.mla_output_project_workspace_size.argtypes = [i32, i32, i32]
+        L.mla_output_project.argtypes = [vp, vp, vp, i32, i32, i32, vp, sz, vp]
         L.mla_decode_noalloc.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, f32, vp, vp]
         for n in ("mla_absorb_q", "mla_absorb_rope_q", "mla_absorb_rope_q_freq", "mla_rope_apply",
                   "mla_rope_apply_freq", "mla_rope_yarn_frequencies", "mla_rope_yarn_softmax_scale",
                   "mla_decode",
                   "mla_splitkv_combine", "mla_up_project", "mla_combine_up_project", "mla_read_status",
-                  "mla_cache_append", "mla_debug_decode_stall",
+                  "mla_cache_append", "mla_debug_decode_stall", "mla_output_project",
                   "mla_decode_noalloc"):
             getattr(L, n).restype = i32
         _lib = L
@@ -309,6 +312,30 @@ def debug_decode_stall(wait_limit_ns: int):
     its bounded waits run out after wait_limit_ns and it reports
     MLA_ERR_TIMEOUT (see mla_debug_decode_stall)."""
     _check(lib().mla_debug_decode_stall(int(wait_limit_ns)), "mla_debug_decode_stall")
+
+
+def output_project_workspace(BS: int, K: int, d: int, device=None):
+    """Workspace for output_project (None when the shape needs none)."""
+    n = int(lib().mla_output_project_workspace_size(BS, K, d))
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda") if n else None
+
+
+def output_project(x, W, u, workspace=None, stream=None):
+    """u[n] = W x[n]: x [BS, K], W [d, K], u [BS, d] (bf16).  With x = out
+    [B,S,H,128] viewed as [B*S, H*128] and W = W^O this is the layer's output
+    projection; with x = o_lat viewed as [B*S, H*512] and W = W^O blockdiag(W^UV)
+    the same projection with the value up-projection folded into W^O."""
+    BS, K = x.shape
+    d = W.shape[0]
+    _need(x, "x", shape=(BS, K))
+    _need(W, "W", shape=(d, K))
+    _need(u, "u", shape=(BS, d))
+    ws, n = ctypes.c_void_p(0), 0
+    if workspace is not None:
+        _need(workspace, "workspace", dtype=torch.uint8)
+        ws, n = _ptr(workspace), workspace.numel()
+    _check(lib().mla_output_project(_ptr(x), _ptr(W), _ptr(u), BS, K, d, ws, n, _stream(stream)),
+           "mla_output_project")
 
 
 def read_status(workspace=None, stream=None) -> int:

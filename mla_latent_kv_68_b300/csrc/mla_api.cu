@@ -20,6 +20,7 @@
 #include "rope.cuh"
 #include "splitkv.cuh"
 #include "up_project.cuh"
+#include "wgemm.cuh"
 
 namespace {
 
@@ -79,7 +80,9 @@ const DeviceInfo* device_info() {
       cudaFuncSetAttribute(mla::combine_up_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)mla::cu_smem_bytes(mla::kCUTile)) != cudaSuccess ||
       cudaFuncSetAttribute(mla::append_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)mla::app_smem_bytes(256)) != cudaSuccess)
+                           (int)mla::app_smem_bytes(256)) != cudaSuccess ||
+      cudaFuncSetAttribute(mla::wgemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)mla::wg_smem_bytes(mla::kWgMaxTile)) != cudaSuccess)
     return nullptr;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -630,6 +633,83 @@ mla_status mla_debug_decode_stall(uint64_t wait_limit_ns) {
   if (wait_limit_ns == 0 || wait_limit_ns > kTimeoutNs) return MLA_ERR_INVALID_ARG;
   g_stall_ns.store(wait_limit_ns);
   return MLA_OK;
+}
+
+}  // extern "C"
+
+namespace {
+
+// Launch shape of the output projection: token tiles of up to 64, weight
+// tiles of 128 rows, and ks near-equal slices of K so that the grid fills the
+// SMs two CTAs deep.
+struct WgPlan {
+  int n_tile = 0, ntiles = 0, mtiles = 0, total_chunks = 0, ks = 1;
+  size_t ws = 0;
+};
+
+WgPlan wg_plan(int BS, int K, int d, int num_sms) {
+  WgPlan w;
+  w.n_tile = BS >= mla::kWgMaxTile ? mla::kWgMaxTile : (BS + 15) / 16 * 16;
+  w.ntiles = (BS + w.n_tile - 1) / w.n_tile;
+  w.mtiles = d / 128;
+  w.total_chunks = K / mla::kWgKc;
+  const long long tiles = (long long)w.mtiles * w.ntiles;
+  w.ks = (int)std::max(1LL, std::min((long long)w.total_chunks, 2LL * num_sms / std::max(1LL, tiles)));
+  w.ws = w.ks > 1 ? sizeof(float) * (size_t)w.ks * BS * d : 0;
+  return w;
+}
+
+bool wg_shape_ok(int BS, int K, int d) {
+  return BS >= 1 && K >= mla::kWgKc && d >= 128 && K % mla::kWgKc == 0 && d % 128 == 0 &&
+         (long long)BS <= 65535LL * mla::kWgMaxTile && (long long)d / 128 <= 0x7fffffffLL && K <= (1 << 24);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t mla_output_project_workspace_size(int BS, int K, int d) {
+  if (!wg_shape_ok(BS, K, d)) return 0;
+  const DeviceInfo* dev = device_info();
+  if (!dev) return 0;
+  return wg_plan(BS, K, d, dev->num_sms).ws;
+}
+
+mla_status mla_output_project(const mla_bf16* x, const mla_bf16* W, mla_bf16* u, int BS, int K, int d,
+                              void* workspace, size_t workspace_bytes, void* stream) {
+  if (!x || !W || !u || !aligned16(x) || !aligned16(W) || !aligned16(u)) return MLA_ERR_INVALID_ARG;
+  if (BS < 1 || K < 1 || d < 1) return MLA_ERR_INVALID_ARG;
+  if (!wg_shape_ok(BS, K, d)) return MLA_ERR_UNSUPPORTED;
+  const DeviceInfo* dev = device_info();
+  if (!dev) return MLA_ERR_CUDA;
+  const WgPlan w = wg_plan(BS, K, d, dev->num_sms);
+  if (w.ws > 0 && (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < w.ws))
+    return MLA_ERR_WORKSPACE;
+  // row-major [rows][K] seen as [64 columns][rows][K / 64 atoms]: one box =
+  // two 128-byte-swizzle atoms of 128 weight rows or n_tile token rows
+  const cuuint64_t str[2] = {(cuuint64_t)K * 2, 128};
+  const cuuint64_t dw[3] = {64, (cuuint64_t)d, (cuuint64_t)(K / 64)}, dx[3] = {64, (cuuint64_t)BS, (cuuint64_t)(K / 64)};
+  const cuuint32_t bw[3] = {64, 128, 2}, bx[3] = {64, (cuuint32_t)w.n_tile, 2};
+  CUtensorMap tw, tx;
+  if (!encode_tiled(&tw, W, 3, dw, str, bw) || !encode_tiled(&tx, x, 3, dx, str, bx)) return MLA_ERR_INVALID_ARG;
+  mla::WGemmParams p;
+  p.part = static_cast<float*>(workspace);
+  p.out = reinterpret_cast<__nv_bfloat16*>(u);
+  p.BS = BS;
+  p.M = d;
+  p.n_tile = w.n_tile;
+  p.ks = w.ks;
+  p.total_chunks = w.total_chunks;
+  p.tmem_cols = pow2_at_least((uint32_t)w.n_tile);
+  p.status = dev->kernel_status;
+  p.timeout_ns = kTimeoutNs;
+  cudaStream_t st = (cudaStream_t)stream;
+  const mla_status s1 = launch_ex(mla::wgemm_kernel, dim3((unsigned)w.mtiles, (unsigned)w.ks, (unsigned)w.ntiles),
+                                  dim3(mla::kWgThreads), mla::wg_smem_bytes(w.n_tile), st, true, 1, tw, tx, p);
+  if (s1 != MLA_OK || w.ks == 1) return s1;
+  const size_t total4 = (size_t)BS * d / 4;
+  return launch_ex(mla::wgemm_reduce_kernel, dim3((unsigned)((total4 + 255) / 256)), dim3(256), 0, st, true, 1,
+                   static_cast<const float*>(workspace), reinterpret_cast<__nv_bfloat16*>(u), BS, d, w.ks);
 }
 
 mla_status mla_read_status(void* workspace, void* stream) {

@@ -18,4 +18,6 @@ from .oracle import (  # noqa: F401
     absorb,
     up_project,
     latent_attention,
+    output_project,
+    fold_output_weights,
 )

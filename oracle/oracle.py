@@ -252,3 +252,26 @@ def latent_attention(q_cat, c_kv, k_rot, seqlens, *, d_r: int, softmax_scale, ro
     if rows is None:
         out = out.reshape(B, S, H, d_c)
     return out
+
+
+def output_project(x, W):
+    """The layer's output projection ("DeepSeek-V3" (ekkoxiao.github.io),
+    "Multi-Head Latent Attention / 注意力计算"): u_t = W^O [o_{t,1}; ...; o_{t,H}].
+    x [N, K] (the heads' outputs of each token, concatenated), W [d, K]
+    (fp64, or uint16 bf16 bits).  Returns u [N, d] in fp64: a plain matrix
+    product (numpy)."""
+    xx, ww = _f64(x), _f64(W)
+    assert xx.ndim == 2 and ww.ndim == 2 and xx.shape[1] == ww.shape[1]
+    return xx @ ww.T
+
+
+def fold_output_weights(W_O, W_UV):
+    """W^O with the value up-projection absorbed ("DeepSeek-V3 技术报告精读"
+    (oopvo.github.io), "MLA": W^UV is absorbed into W^O): since
+    o_i = W_i^UV o_lat_i, W^O [o_1; ...; o_H] = W~ [o_lat_1; ...; o_lat_H] with
+    W~[:, i d_c:(i+1) d_c] = W^O[:, i d_v:(i+1) d_v] W_i^UV.
+    W_O [d, H d_v], W_UV [H, d_v, d_c].  Returns W~ [d, H d_c] in fp64."""
+    wo, wv = _f64(W_O), _f64(W_UV)
+    H, d_v, d_c = wv.shape
+    assert wo.shape[1] == H * d_v
+    return np.concatenate([wo[:, i * d_v:(i + 1) * d_v] @ wv[i] for i in range(H)], axis=1)

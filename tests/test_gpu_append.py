@@ -103,3 +103,17 @@ def test_cache_append_reports_a_position_past_the_cache():
     assert mb.read_status(ws) == mb.MLA_ERR_BAD_SEQLEN
     assert mb.read_status(ws) == mb.MLA_OK   # reading clears it
     _check(c, k, h, wd, wr, [10, 1, 64], skip=(1,))
+
+
+def test_cache_append_twice_with_one_workspace():
+    # a workspace serves call after call: nothing of the first call's partial
+    # products leaks into the second's result
+    B, S, d, seqlens, Lmax = 4, 2, 1024, [2, 50, 300, 9], 320
+    ws = mb.cache_append_workspace(B, S, d)
+    for seed in (21, 22):
+        h, wd, wr = _case(B, S, d, seed=seed)
+        c = torch.full((B, Lmax, 512), SENTINEL, dtype=torch.bfloat16, device="cuda")
+        k = torch.full((B, Lmax, 64), SENTINEL, dtype=torch.bfloat16, device="cuda")
+        mb.cache_append(h.cuda(), wd.cuda(), wr.cuda(), torch.tensor(seqlens, dtype=torch.int32).cuda(), c, k, ws)
+        assert mb.read_status(ws) == mb.MLA_OK
+        _check(c, k, h, wd, wr, seqlens)
