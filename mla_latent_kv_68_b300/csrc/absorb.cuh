@@ -90,17 +90,36 @@ __global__ void __launch_bounds__(kAbsorbThreads, 1)
     }
   }
 
-  // The query RoPE (one of the two k-halves does it) overlaps the weight load.
+  // The query RoPE overlaps the weight load: the two k-halves' CTAs share it,
+  // warps 1..3 do it (warp 0 issues the MMA as soon as the weight lands), and
+  // each thread requests all its rows' positions and values before it
+  // computes, so the loads cost one memory round trip rather than one each.
   const int nvalid = min(p.n_tile, p.BS - n0);
-  if (p.q_rope != nullptr && half == 1) {
-    for (int it = threadIdx.x; it < nvalid * 8; it += kAbsorbThreads) {
-      const int n = n0 + (it >> 3), part = it & 7;
-      const int b = n / p.S, s = n - b * p.S;
-      const int64_t pos = (int64_t)p.seqlens[b] - p.S + s;
-      if (pos < 0) continue;
-      const uint4 v = *reinterpret_cast<const uint4*>(p.q_rope + ((size_t)n * p.H + h) * 64 + part * 8);
-      *reinterpret_cast<uint4*>(p.q_cat + ((size_t)n * p.H + h) * 576 + 512 + part * 8) =
-          rope_rotate4(v, pos, part, th);
+  if (p.q_rope != nullptr && warp >= 1) {
+    constexpr int kRopeThreads = kAbsorbThreads - 32, kRopeBatch = 6;
+    const int items = nvalid * 8, lo = half == 0 ? 0 : items / 2, hi = half == 0 ? items / 2 : items;
+    for (int base = lo + (int)threadIdx.x - 32; base < hi; base += kRopeThreads * kRopeBatch) {
+      int64_t pos[kRopeBatch];
+      uint4 v[kRopeBatch];
+#pragma unroll
+      for (int u = 0; u < kRopeBatch; ++u) {
+        const int it = base + u * kRopeThreads;
+        pos[u] = -1;
+        if (it < hi) {
+          const int n = n0 + (it >> 3), b = n / p.S, s = n - b * p.S;
+          pos[u] = (int64_t)p.seqlens[b] - p.S + s;
+          v[u] = *reinterpret_cast<const uint4*>(p.q_rope + ((size_t)n * p.H + h) * 64 + (it & 7) * 8);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kRopeBatch; ++u) {
+        const int it = base + u * kRopeThreads;
+        if (it < hi && pos[u] >= 0) {
+          const int n = n0 + (it >> 3);
+          *reinterpret_cast<uint4*>(p.q_cat + ((size_t)n * p.H + h) * 576 + 512 + (it & 7) * 8) =
+              rope_rotate4(v[u], pos[u], it & 7, th);
+        }
+      }
     }
   }
 
