@@ -34,6 +34,15 @@
  *     recorded in the decode workspace and returned by mla_read_status.
  *   - Query positions are 0-based: keys sit at 0..L_b-1 and query s of S at
  *     L_b - S + s, which sees keys 0..L_b - S + s.
+ *   - Kernels after the first of a step start before their predecessor has
+ *     finished (programmatic dependent launch).  Each waits for it before
+ *     reading that kernel's output, but weights (W_UV, W^O, W^DKV, W^KR) may
+ *     stream in earlier: a weight must not be written by the kernel launched
+ *     immediately before the call that reads it on the same stream.
+ *   - The library keeps, per device, the device properties, its function
+ *     attributes and the address of its scratch array, found on the first
+ *     call on that device.  After cudaDeviceReset on a device, no call of
+ *     this library may run on that device again in the same process.
  */
 #ifndef MLA_H
 #define MLA_H
@@ -208,6 +217,8 @@ mla_status mla_splitkv_combine(const void *workspace, size_t workspace_bytes, ml
  * fp32 accumulation on the tensor cores, rounded to bf16.
  *   o_lat [B,S,H,512] bf16,  W_UV [H,128,512] bf16 (W_UV[h][v][k]),
  *   out   [B,S,H,128] bf16 output (per-head output before W^O).
+ * W_UV is read before the kernel waits for the one launched before it, so it
+ * must not be written by that kernel.
  */
 mla_status mla_up_project(const mla_bf16 *o_lat, const mla_bf16 *W_UV, mla_bf16 *out, int B,
                           int S, int H, void *stream);

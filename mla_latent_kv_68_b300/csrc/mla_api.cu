@@ -117,9 +117,9 @@ bool encode_tiled(CUtensorMap* map, const void* base, cuuint32_t rank, const cuu
 }
 
 // Tensor maps of the decode kernel: the score CTA reads 128-row boxes of c
-// and q_cat (two 64-column blocks, 32 KB) and of k^R and q^R, the value CTA
-// 64-row boxes of c (all eight blocks, 64 KB); a block is 64 columns = 128
-// bytes, one 128-byte-swizzle atom.
+// and q_cat (four 64-column blocks, 64 KB) and of k^R and q^R (16 KB), the
+// value CTA 32-row boxes of c (all eight blocks, 32 KB); a block is 64
+// columns = 128 bytes, one 128-byte-swizzle atom.
 struct DecodeMaps {
   CUtensorMap c0, kr, q, qr, c1;
 };
