@@ -354,6 +354,7 @@ def measure_workload(name, args, world, dev, stream, flush_l2, mb, headline=Fals
         r["h2d"], r["d2h"] = pk.nbytes, hout.numel() * 2
         r["append"] = _time_append(args, x, d, dev, stream, flush_l2, theta, mb)
         r["oproj"] = _time_output_project(args, x, dev, stream, flush_l2, mb)
+        r["prefill"] = _time_prefill(args, dev, stream, flush_l2, mb)
     del g_all, g_q, g_a, g_p, step, d, pk
     torch.cuda.empty_cache()
     return r
@@ -391,6 +392,63 @@ def _time_output_project(args, x, dev, stream, flush_l2, mb):
     torch.cuda.empty_cache()
     return {"workload": f"{BS} tokens, W^O [{APPEND_D}, {K}]", "us": round(us, 3), "bytes": nbytes,
             "launches": 2}
+
+
+PREFILL = dict(name="prefill_b4_s4096_h128", B=4, S=4096, H=128)
+
+
+def _time_prefill(args, dev, stream, flush_l2, mb):
+    """Prefill of whole prompts (not part of the decode step): B prompts of S
+    tokens, every position querying the cache up to itself.  Times the three
+    phases (RoPE of the queries, expansion of keys and values per head, causal
+    attention) in one graph, and the attention alone in another, each after an
+    L2 flush.  Algorithmic flops: 2 x 2 x (B S) x (H 128) x 512 for the
+    expansion and 2 x (192 + 128) x H per visible (query, key) pair."""
+    from mla_latent_kv_68_b300.inputs import make_inputs
+    B, S, H = PREFILL["B"], PREFILL["S"], PREFILL["H"]
+    x = make_inputs(B, S, H, [S] * B, seed=68005)
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    mb.rope_cache(d["k_r"], d["seqlens"])
+    step = mb.PrefillStep(B, S, H, S, device=dev)
+    run = lambda: step(d["q_nope"], d["q_rope"], d["c_kv"], d["k_r"], d["seqlens"], d["W_UK"], d["W_UV"])
+    attn = lambda: mb.prefill_attention(d["q_nope"], step.q_rot, step.k_c, d["k_r"], step.v_c, d["seqlens"],
+                                        step.out)
+    for _ in range(max(3, args.warmup)):
+        run()
+    graphs = []
+    for fn in (run, attn):
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr):
+            fn()
+        graphs.append(gr)
+    times = []
+    for gr in graphs:
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(min(args.steps, 10))]
+        torch.cuda.synchronize(dev)
+        for e in ev:
+            flush_l2()
+            e[0].record(stream)
+            gr.replay()
+            e[1].record(stream)
+        torch.cuda.synchronize(dev)
+        times.append(statistics.mean(e[0].elapsed_time(e[1]) for e in ev) * 1000)
+    if mb.read_status() != mb.MLA_OK:
+        raise RuntimeError("device status not clean after the prefill")
+    pairs = B * H * S * (S + 1) // 2
+    f_attn = pairs * 2 * (192 + 128)
+    f_exp = 2 * 2 * B * S * H * 128 * 512
+    _, tf_burst, _, _ = _peaks()
+    del graphs, step, d, x
+    torch.cuda.empty_cache()
+    total_us, attn_us = times
+    return {"workload": f"{PREFILL['name']}: {B} prompts of {S} tokens, {H} heads, causal",
+            "us": round(total_us, 3), "attention_us": round(attn_us, 3),
+            "flops": f_attn + f_exp, "attention_flops": f_attn,
+            "tflops": round((f_attn + f_exp) / (total_us * 1e-6) / 1e12, 1),
+            "attention_tflops": round(f_attn / (attn_us * 1e-6) / 1e12, 1),
+            "frac": round((f_attn + f_exp) / (total_us * 1e-6) / 1e12 / tf_burst, 4),
+            "attention_frac": round(f_attn / (attn_us * 1e-6) / 1e12 / tf_burst, 4),
+            "peak_tflops": tf_burst, "launches": 4}
 
 
 def run_ours(args, rank, world, local_rank):
@@ -475,6 +533,7 @@ def run_ours(args, rank, world, local_rank):
         "output_projection": {**r["oproj"],
                               "achieved_gbs": round(r["oproj"]["bytes"] / (r["oproj"]["us"] * 1e-6) / 1e9, 1),
                               "frac": round(r["oproj"]["bytes"] / (r["oproj"]["us"] * 1e-6) / 1e9 / hbm, 4)},
+        "prefill": r["prefill"],
         "gpu_launches": mb.DecodeStep.LAUNCHES_PER_STEP * args.steps,
         "clocks": clocks.summary(),
     }

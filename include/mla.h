@@ -294,6 +294,47 @@ mla_status mla_output_project(const mla_bf16 *x, const mla_bf16 *W, mla_bf16 *u,
                               void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Prefill, step 1: the keys and values of every cached token expanded per
+ * head ("KeyValue": k^C_{t,i} = W_i^UK c_t, v^C_{t,i} = W_i^UV c_t), fp32
+ * accumulation on the tensor cores, rounded to bf16:
+ *   c_kv  [B,Lmax,512] bf16 (every row is expanded; rows past a sequence's
+ *         length may hold anything, mla_prefill_attention never uses them)
+ *   W_UK, W_UV [H,128,512] bf16
+ *   k_c, v_c   [B,Lmax,H,128] bf16 outputs
+ * Requires 1 <= H <= 128 and B * Lmax <= 4,194,240.  Two launches (one per
+ * weight); the weights may stream in before the kernel launched before this
+ * call has finished, so they must not be written by that kernel.
+ * Device-side errors go to the library status word.
+ */
+mla_status mla_prefill_expand(const mla_bf16 *c_kv, const mla_bf16 *W_UK, const mla_bf16 *W_UV,
+                              mla_bf16 *k_c, mla_bf16 *v_c, int B, int Lmax, int H, void *stream);
+
+/*
+ * Prefill, step 2: causal attention of S new query positions per sequence
+ * over the expanded keys and values ("注意力计算"):
+ *   o_{t,h} = sum_{j <= t} a_j v^C_{j,h},
+ *   a = softmax_j((q^C_{t,h} . k^C_{j,h} + q^R_{t,h} . k^R_j) * softmax_scale)
+ * for query s of sequence b at position t = seqlens[b] - S + s (the mla_decode
+ * rule; S = seqlens[b] is a whole prompt, a smaller S a chunk after cached
+ * context), with fp32 scores, P rounded to bf16, fp32 accumulation:
+ *   q_nope  [B,S,H,128] bf16,
+ *   q_rope  [B,S,H,64] bf16, ALREADY rotated at the query positions
+ *           (mla_rope_apply with MLA_POS_QUERY and group = S),
+ *   k_c, v_c [B,Lmax,H,128] bf16 from mla_prefill_expand,
+ *   k_r     [B,Lmax,64] bf16, the cache's rotated keys,
+ *   seqlens [B] int32 device, S <= seqlens[b] <= Lmax,
+ *   softmax_scale  1/sqrt(192) (or the YaRN factor times it),
+ *   out     [B,S,H,128] bf16 output (per-head output before W^O).
+ * Requires 1 <= H <= 128 and 1 <= S <= Lmax.  A sequence whose length is out
+ * of range sets MLA_ERR_BAD_SEQLEN in the library status word and its rows of
+ * `out` are not written.  Cache rows at or past seqlens[b] are never used,
+ * whatever they hold.
+ */
+mla_status mla_prefill_attention(const mla_bf16 *q_nope, const mla_bf16 *q_rope, const mla_bf16 *k_c,
+                                 const mla_bf16 *k_r, const mla_bf16 *v_c, const int32_t *seqlens, int B,
+                                 int S, int H, int Lmax, float softmax_scale, mla_bf16 *out, void *stream);
+
+/*
  * Test hook for the kernels' bounded waits.  The next mla_decode call (only
  * that one) launches with its split-plan barrier left incomplete: every warp
  * that waits on it gives up after wait_limit_ns nanoseconds (instead of the

@@ -76,12 +76,14 @@ def lib():
         L.mla_output_project_workspace_size.argtypes = [i32, i32, i32]
         L.mla_output_project.argtypes = [vp, vp, vp, i32, i32, i32, vp, sz, vp]
         L.mla_decode_noalloc.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, f32, vp, vp]
+        L.mla_prefill_expand.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, vp]
+        L.mla_prefill_attention.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, vp, vp]
         for n in ("mla_absorb_q", "mla_absorb_rope_q", "mla_absorb_rope_q_freq", "mla_rope_apply",
                   "mla_rope_apply_freq", "mla_rope_yarn_frequencies", "mla_rope_yarn_softmax_scale",
                   "mla_decode",
                   "mla_splitkv_combine", "mla_up_project", "mla_combine_up_project", "mla_read_status",
                   "mla_cache_append", "mla_debug_decode_stall", "mla_output_project",
-                  "mla_decode_noalloc"):
+                  "mla_decode_noalloc", "mla_prefill_expand", "mla_prefill_attention"):
             getattr(L, n).restype = i32
         _lib = L
     return _lib
@@ -336,6 +338,66 @@ def output_project(x, W, u, workspace=None, stream=None):
         ws, n = _ptr(workspace), workspace.numel()
     _check(lib().mla_output_project(_ptr(x), _ptr(W), _ptr(u), BS, K, d, ws, n, _stream(stream)),
            "mla_output_project")
+
+
+def rope_prefill_queries(q_rope, q_rot, seqlens, base=ROPE_BASE, stream=None, theta=None):
+    """q_rot [B,S,H,64] = RoPE(q_rope) at positions seqlens[b] - S + s."""
+    B, S, H, _ = q_rope.shape
+    _need(q_rope, "q_rope", shape=(B, S, H, D_R))
+    _need(q_rot, "q_rot", shape=(B, S, H, D_R))
+    _need(seqlens, "seqlens", dtype=torch.int32, shape=(B,))
+    rope_apply(q_rope, H * D_R, D_R, q_rot, H * D_R, D_R, B * S, H, POS_QUERY, seqlens, S, base,
+               stream, theta)
+
+
+def prefill_expand(c_kv, W_UK, W_UV, k_c, v_c, stream=None):
+    """k_c / v_c [B,Lmax,H,128] = W_UK[h] c_t / W_UV[h] c_t for every cache row."""
+    B, Lmax, _ = c_kv.shape
+    H = W_UK.shape[0]
+    _need(c_kv, "c_kv", shape=(B, Lmax, D_C))
+    _need(W_UK, "W_UK", shape=(H, D_H, D_C))
+    _need(W_UV, "W_UV", shape=(H, D_V, D_C))
+    _need(k_c, "k_c", shape=(B, Lmax, H, D_H))
+    _need(v_c, "v_c", shape=(B, Lmax, H, D_V))
+    _check(lib().mla_prefill_expand(_ptr(c_kv), _ptr(W_UK), _ptr(W_UV), _ptr(k_c), _ptr(v_c), B, Lmax, H,
+                                    _stream(stream)), "mla_prefill_expand")
+
+
+def prefill_attention(q_nope, q_rot, k_c, k_r, v_c, seqlens, out, softmax_scale=SOFTMAX_SCALE, stream=None):
+    """Causal attention of the S queries per sequence over the expanded keys
+    and values: out [B,S,H,128].  q_rot is the rotated q^R (rope_prefill_queries)."""
+    B, S, H, _ = q_nope.shape
+    Lmax = k_r.shape[1]
+    _need(q_nope, "q_nope", shape=(B, S, H, D_H))
+    _need(q_rot, "q_rot", shape=(B, S, H, D_R))
+    _need(k_c, "k_c", shape=(B, Lmax, H, D_H))
+    _need(k_r, "k_r", shape=(B, Lmax, D_R))
+    _need(v_c, "v_c", shape=(B, Lmax, H, D_V))
+    _need(seqlens, "seqlens", dtype=torch.int32, shape=(B,))
+    _need(out, "out", shape=(B, S, H, D_V))
+    _check(lib().mla_prefill_attention(_ptr(q_nope), _ptr(q_rot), _ptr(k_c), _ptr(k_r), _ptr(v_c), _ptr(seqlens),
+                                       B, S, H, Lmax, softmax_scale, _ptr(out), _stream(stream)),
+           "mla_prefill_attention")
+
+
+class PrefillStep:
+    """Buffers and calls of one prefill shape: RoPE of the queries, expansion
+    of the cached keys and values per head, causal attention."""
+
+    def __init__(self, B: int, S: int, H: int, Lmax: int, device="cuda"):
+        self.B, self.S, self.H, self.Lmax = B, S, H, Lmax
+        bf = torch.bfloat16
+        self.q_rot = torch.empty(B, S, H, D_R, dtype=bf, device=device)
+        self.k_c = torch.empty(B, Lmax, H, D_H, dtype=bf, device=device)
+        self.v_c = torch.empty(B, Lmax, H, D_V, dtype=bf, device=device)
+        self.out = torch.empty(B, S, H, D_V, dtype=bf, device=device)
+
+    def __call__(self, q_nope, q_rope, c_kv, k_r, seqlens, W_UK, W_UV, softmax_scale=SOFTMAX_SCALE,
+                 theta=None, stream=None):
+        rope_prefill_queries(q_rope, self.q_rot, seqlens, stream=stream, theta=theta)
+        prefill_expand(c_kv, W_UK, W_UV, self.k_c, self.v_c, stream=stream)
+        prefill_attention(q_nope, self.q_rot, self.k_c, k_r, self.v_c, seqlens, self.out, softmax_scale, stream)
+        return self.out
 
 
 def read_status(workspace=None, stream=None) -> int:

@@ -17,6 +17,7 @@
 #include "append.cuh"
 #include "combine_up.cuh"
 #include "decode.cuh"
+#include "prefill.cuh"
 #include "rope.cuh"
 #include "splitkv.cuh"
 #include "up_project.cuh"
@@ -82,7 +83,9 @@ const DeviceInfo* device_info() {
       cudaFuncSetAttribute(mla::append_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)mla::app_smem_bytes(256)) != cudaSuccess ||
       cudaFuncSetAttribute(mla::wgemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)mla::wg_smem_bytes(mla::kWgMaxTile)) != cudaSuccess)
+                           (int)mla::wg_smem_bytes(mla::kWgMaxTile)) != cudaSuccess ||
+      cudaFuncSetAttribute(mla::prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)mla::kPfSmem) != cudaSuccess)
     return nullptr;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -647,14 +650,14 @@ struct WgPlan {
   size_t ws = 0;
 };
 
-WgPlan wg_plan(int BS, int K, int d, int num_sms) {
+WgPlan wg_plan(int BS, int K, int d, int num_sms, bool split = true) {
   WgPlan w;
   w.n_tile = BS >= mla::kWgMaxTile ? mla::kWgMaxTile : (BS + 15) / 16 * 16;
   w.ntiles = (BS + w.n_tile - 1) / w.n_tile;
   w.mtiles = d / 128;
   w.total_chunks = K / mla::kWgKc;
   const long long tiles = (long long)w.mtiles * w.ntiles;
-  w.ks = (int)std::max(1LL, std::min((long long)w.total_chunks, 2LL * num_sms / std::max(1LL, tiles)));
+  w.ks = split ? (int)std::max(1LL, std::min((long long)w.total_chunks, 2LL * num_sms / std::max(1LL, tiles))) : 1;
   w.ws = w.ks > 1 ? sizeof(float) * (size_t)w.ks * BS * d : 0;
   return w;
 }
@@ -664,27 +667,9 @@ bool wg_shape_ok(int BS, int K, int d) {
          (long long)BS <= 65535LL * mla::kWgMaxTile && (long long)d / 128 <= 0x7fffffffLL && K <= (1 << 24);
 }
 
-}  // namespace
-
-extern "C" {
-
-size_t mla_output_project_workspace_size(int BS, int K, int d) {
-  if (!wg_shape_ok(BS, K, d)) return 0;
-  const DeviceInfo* dev = device_info();
-  if (!dev) return 0;
-  return wg_plan(BS, K, d, dev->num_sms).ws;
-}
-
-mla_status mla_output_project(const mla_bf16* x, const mla_bf16* W, mla_bf16* u, int BS, int K, int d,
-                              void* workspace, size_t workspace_bytes, void* stream) {
-  if (!x || !W || !u || !aligned16(x) || !aligned16(W) || !aligned16(u)) return MLA_ERR_INVALID_ARG;
-  if (BS < 1 || K < 1 || d < 1) return MLA_ERR_INVALID_ARG;
-  if (!wg_shape_ok(BS, K, d)) return MLA_ERR_UNSUPPORTED;
-  const DeviceInfo* dev = device_info();
-  if (!dev) return MLA_ERR_CUDA;
-  const WgPlan w = wg_plan(BS, K, d, dev->num_sms);
-  if (w.ws > 0 && (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < w.ws))
-    return MLA_ERR_WORKSPACE;
+// u = W x through wgemm_kernel (and the slice reduction when w.ks > 1).
+mla_status wg_launch(const mla_bf16* x, const mla_bf16* W, mla_bf16* u, int BS, int K, int d, const WgPlan& w,
+                     const DeviceInfo* dev, void* workspace, void* stream) {
   // row-major [rows][K] seen as [64 columns][rows][K / 64 atoms]: one box =
   // two 128-byte-swizzle atoms of 128 weight rows or n_tile token rows
   const cuuint64_t str[2] = {(cuuint64_t)K * 2, 128};
@@ -710,6 +695,94 @@ mla_status mla_output_project(const mla_bf16* x, const mla_bf16* W, mla_bf16* u,
   const size_t total4 = (size_t)BS * d / 4;
   return launch_ex(mla::wgemm_reduce_kernel, dim3((unsigned)((total4 + 255) / 256)), dim3(256), 0, st, true, 1,
                    static_cast<const float*>(workspace), reinterpret_cast<__nv_bfloat16*>(u), BS, d, w.ks);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t mla_output_project_workspace_size(int BS, int K, int d) {
+  if (!wg_shape_ok(BS, K, d)) return 0;
+  const DeviceInfo* dev = device_info();
+  if (!dev) return 0;
+  return wg_plan(BS, K, d, dev->num_sms).ws;
+}
+
+mla_status mla_output_project(const mla_bf16* x, const mla_bf16* W, mla_bf16* u, int BS, int K, int d,
+                              void* workspace, size_t workspace_bytes, void* stream) {
+  if (!x || !W || !u || !aligned16(x) || !aligned16(W) || !aligned16(u)) return MLA_ERR_INVALID_ARG;
+  if (BS < 1 || K < 1 || d < 1) return MLA_ERR_INVALID_ARG;
+  if (!wg_shape_ok(BS, K, d)) return MLA_ERR_UNSUPPORTED;
+  const DeviceInfo* dev = device_info();
+  if (!dev) return MLA_ERR_CUDA;
+  const WgPlan w = wg_plan(BS, K, d, dev->num_sms);
+  if (w.ws > 0 && (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < w.ws))
+    return MLA_ERR_WORKSPACE;
+  return wg_launch(x, W, u, BS, K, d, w, dev, workspace, stream);
+}
+
+mla_status mla_prefill_expand(const mla_bf16* c_kv, const mla_bf16* W_UK, const mla_bf16* W_UV, mla_bf16* k_c,
+                              mla_bf16* v_c, int B, int Lmax, int H, void* stream) {
+  if (!c_kv || !W_UK || !W_UV || !k_c || !v_c || !aligned16(c_kv) || !aligned16(W_UK) || !aligned16(W_UV) ||
+      !aligned16(k_c) || !aligned16(v_c))
+    return MLA_ERR_INVALID_ARG;
+  if (B < 1 || Lmax < 1 || H < 1) return MLA_ERR_INVALID_ARG;
+  const long long rows = (long long)B * Lmax;
+  if (H > 128 || rows > 65535LL * mla::kWgMaxTile) return MLA_ERR_UNSUPPORTED;
+  const DeviceInfo* dev = device_info();
+  if (!dev) return MLA_ERR_CUDA;
+  // k^C[t][h][:] = W_UK[h] c_t: the GEMM u = W x with x = the cache rows
+  // [B*Lmax][512] and W = W_UK seen as [H*128][512]; v^C likewise with W_UV.
+  const int d = H * 128;
+  const WgPlan w = wg_plan((int)rows, MLA_D_C, d, dev->num_sms, false);
+  const mla_status s1 = wg_launch(c_kv, W_UK, k_c, (int)rows, MLA_D_C, d, w, dev, nullptr, stream);
+  if (s1 != MLA_OK) return s1;
+  return wg_launch(c_kv, W_UV, v_c, (int)rows, MLA_D_C, d, w, dev, nullptr, stream);
+}
+
+mla_status mla_prefill_attention(const mla_bf16* q_nope, const mla_bf16* q_rope, const mla_bf16* k_c,
+                                 const mla_bf16* k_r, const mla_bf16* v_c, const int32_t* seqlens, int B, int S,
+                                 int H, int Lmax, float softmax_scale, mla_bf16* out, void* stream) {
+  if (!q_nope || !q_rope || !k_c || !k_r || !v_c || !seqlens || !out || !aligned16(q_nope) || !aligned16(q_rope) ||
+      !aligned16(k_c) || !aligned16(k_r) || !aligned16(v_c) || !aligned16(out))
+    return MLA_ERR_INVALID_ARG;
+  if (B < 1 || S < 1 || H < 1 || Lmax < 1 || S > Lmax || !(softmax_scale > 0.f) || !std::isfinite(softmax_scale))
+    return MLA_ERR_INVALID_ARG;
+  const int nq = (S + 127) / 128;
+  if (H > 128 || (long long)B * Lmax + 128 > 0x7fffffffLL || (long long)B * S + 128 > 0x7fffffffLL ||
+      (long long)B * H * nq > 0x7fffffffLL)
+    return MLA_ERR_UNSUPPORTED;
+  const DeviceInfo* dev = device_info();
+  if (!dev) return MLA_ERR_CUDA;
+  // [rows][H][128] seen as [64 columns][rows][2 atoms][H]: one box = the two
+  // 128-byte-swizzle atoms of 128 rows of one head; [rows][H][64] and
+  // [rows][64] likewise with one atom.
+  const cuuint64_t qrows = (cuuint64_t)B * S, krows = (cuuint64_t)B * Lmax, hh = (cuuint64_t)H;
+  const cuuint64_t dq[4] = {64, qrows, 2, hh}, dk[4] = {64, krows, 2, hh};
+  const cuuint64_t s4[3] = {hh * 256, 128, 256};
+  const cuuint64_t dqr[3] = {64, qrows, hh}, sqr[2] = {hh * 128, 128};
+  const cuuint64_t dkr[2] = {64, krows}, skr[1] = {128};
+  const cuuint32_t b4[4] = {64, 128, 2, 1}, b3[3] = {64, 128, 1}, b2[2] = {64, 128};
+  CUtensorMap tqn, tqr, tkc, tkr, tvc;
+  if (!encode_tiled(&tqn, q_nope, 4, dq, s4, b4) || !encode_tiled(&tqr, q_rope, 3, dqr, sqr, b3) ||
+      !encode_tiled(&tkc, k_c, 4, dk, s4, b4) || !encode_tiled(&tkr, k_r, 2, dkr, skr, b2) ||
+      !encode_tiled(&tvc, v_c, 4, dk, s4, b4))
+    return MLA_ERR_INVALID_ARG;
+  mla::PrefillParams p;
+  p.out = reinterpret_cast<__nv_bfloat16*>(out);
+  p.seqlens = seqlens;
+  p.B = B;
+  p.S = S;
+  p.H = H;
+  p.Lmax = Lmax;
+  p.nq = nq;
+  p.n_items = B * H * nq;
+  p.scale_log2 = (float)((double)softmax_scale * 1.4426950408889634);
+  p.status = dev->kernel_status;
+  p.timeout_ns = kTimeoutNs;
+  const int grid = std::min(p.n_items, dev->num_sms);
+  return launch_ex(mla::prefill_kernel, dim3((unsigned)grid), dim3(mla::kPfThreads), mla::kPfSmem,
+                   (cudaStream_t)stream, true, 1, tqn, tqr, tkc, tkr, tvc, p);
 }
 
 mla_status mla_read_status(void* workspace, void* stream) {

@@ -1,0 +1,384 @@
+// prefill.cuh -- causal attention of many query positions per sequence
+// (prefill and long chunks), in the expanded form.
+//
+// "DeepSeek-V3" (ekkoxiao.github.io), "Multi-Head Latent Attention":
+//   KeyValue:  k^C_{t,i} = W_i^UK c_t,  v^C_{t,i} = W_i^UV c_t,  k^R_t = RoPE_t(.)
+//   Query:     q_{t,i} = [q^C_{t,i}; q^R_{t,i}]  (q^R rotated at t)
+//   注意力计算: o_{t,i} = sum_{j <= t} softmax_j(q_{t,i} . [k^C_{j,i}; k^R_j] / sqrt(192)) v^C_{j,i}
+// When every position of a prompt queries the cache, expanding the keys and
+// values once per head (mla_prefill_expand: 2 x 128 x 512 x 2 flops per token
+// and head) makes each (query, key, head) cost 2 x (192 + 128) flops, where the
+// absorbed form of "潜在向量的作用" costs 2 x (576 + 512).
+//
+// A work item is 128 consecutive query positions of one (sequence, head); its
+// rows see keys 0 .. their own position, so the item walks key tiles of 128
+// from the start of the sequence to the tile holding its last position.  One
+// persistent CTA per SM takes items round-robin (heaviest first within each
+// head, and the items of one head next to each other, so that a head's
+// expanded keys and values are read from HBM about once and then from L2).
+//
+// Per CTA (256 threads): warp 0 issues TMA copies (Q once per item: q^C and
+// q^R as three 128-byte-swizzle atoms; per key tile: k^C, k^R, v^C), warp 1
+// issues the MMAs (one thread), warps 4..7 run the online softmax, one row per
+// thread, and the epilogue; warps 2..3 only take part in set-up and wind-down.
+// Tensor memory holds three 128-column score buffers S and the 128 x 128 fp32
+// output O (columns 384..511).  QK^T of tile t + 1 runs while the softmax
+// works on tile t; the softmax writes P (bf16) over the first half of each
+// 64-column half of its S buffer and P.V reads it from there (A operand in
+// tensor memory).  The online softmax keeps an integer reference exponent per
+// row (log2 units) that moves only when a tile's maximum passes it by more
+// than 8, so every rescale of O and of the row sum is an exact power of two.
+#pragma once
+
+#include "sm100.cuh"
+
+namespace mla {
+
+constexpr int kPfThreads = 256;
+constexpr int kPfAtom = 128 * 128;  // 128 rows x 64 bf16 columns (one swizzle atom column), 16 KB
+constexpr int kPfQ = 3 * kPfAtom;   // q^C (two atoms) + q^R (one)
+constexpr int kPfK = 3 * kPfAtom;   // k^C (two atoms) + k^R (one)
+constexpr int kPfV = 2 * kPfAtom;   // v^C (two atoms)
+constexpr int kPfKStages = 2, kPfVStages = 2;
+constexpr int kPfOffK = kPfQ;
+constexpr int kPfOffV = kPfOffK + kPfKStages * kPfK;
+constexpr int kPfOffBar = kPfOffV + kPfVStages * kPfV;
+enum : int {
+  PF_QFULL = 0, PF_QEMPTY = 1, PF_KFULL = 2, PF_KEMPTY = 4, PF_VFULL = 6, PF_VEMPTY = 8,
+  PF_SFULL = 10, PF_PREADY = 13, PF_PVDONE = 16, PF_OFREE = 19, PF_DRAIN = 20, PF_NBARS = 21
+};
+constexpr size_t kPfSmem = (size_t)kPfOffBar + PF_NBARS * 8 + 16;
+constexpr uint32_t kPfOCol = 384;  // O; the score buffers sit at columns 0, 128 and 256
+
+struct PrefillParams {
+  __nv_bfloat16* out;        // [B, S, H, 128]
+  const int32_t* seqlens;    // [B]: cached tokens, the S new ones included
+  int B, S, H, Lmax;
+  int nq;                    // query blocks of 128 per (sequence, head)
+  int n_items;               // B * H * nq
+  float scale_log2;          // softmax scale * log2(e)
+  uint32_t* status;
+  uint64_t timeout_ns;
+};
+
+struct PfItem {
+  int b, h, s0, nrow, p0, p_last, nt;
+  bool ok;
+};
+
+// Item i: head-major (b, h), and within a head the query blocks from the last
+// (the most key tiles) to the first.
+__device__ __forceinline__ PfItem pf_item(const PrefillParams& p, int i) {
+  PfItem it;
+  const int bh = i / p.nq;
+  const int qb = p.nq - 1 - (i - bh * p.nq);
+  it.b = bh / p.H;
+  it.h = bh - it.b * p.H;
+  const int L = __ldg(p.seqlens + it.b);
+  it.ok = L >= p.S && L <= p.Lmax;
+  it.s0 = qb * 128;
+  it.nrow = min(128, p.S - it.s0);
+  it.p0 = L - p.S + it.s0;            // position of the block's first query
+  it.p_last = it.p0 + it.nrow - 1;    // and of its last (at most L - 1)
+  it.nt = it.ok ? it.p_last / 128 + 1 : 0;
+  return it;
+}
+
+__device__ __forceinline__ bool pf_warp_wait(uint64_t* bar, uint32_t parity, const WaitCtx& w) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, w));
+}
+
+// Exact 2^d for an integer d <= 0 (0 below the normal range).
+__device__ __forceinline__ float pf_exp2_int(int d) {
+  return d <= -127 ? 0.f : __int_as_float((127 + d) << 23);
+}
+
+__global__ void __launch_bounds__(kPfThreads, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap tm_qn, const __grid_constant__ CUtensorMap tm_qr,
+                   const __grid_constant__ CUtensorMap tm_kc, const __grid_constant__ CUtensorMap tm_kr,
+                   const __grid_constant__ CUtensorMap tm_vc, const PrefillParams p) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kPfOffBar);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + PF_NBARS);
+  volatile uint32_t* abort_flag = tmem_slot + 1;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const WaitCtx wc{abort_flag, p.status, p.timeout_ns};
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0u;
+    for (int i = 0; i < PF_NBARS; ++i) {
+      const bool per_thread = (i >= PF_PREADY && i < PF_PREADY + 3) || i == PF_OFREE;
+      mbar_init(&bar[i], per_thread ? 128u : 1u);
+    }
+    fence_mbar_init_cluster();
+    tma_prefetch_desc(&tm_qn);
+    tma_prefetch_desc(&tm_qr);
+    tma_prefetch_desc(&tm_kc);
+    tma_prefetch_desc(&tm_kr);
+    tma_prefetch_desc(&tm_vc);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  pdl_trigger();
+  pdl_wait();  // q, the expanded keys and values and the cache come from earlier kernels
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ TMA producer
+      uint32_t kc = 0, vc = 0, it = 0, q_issued = 0;
+      bool ok = true;
+      for (int i = blockIdx.x; ok && i < p.n_items; i += gridDim.x) {
+        const PfItem ii = pf_item(p, i);
+        if (!ii.ok) {
+          atomicOr(p.status, kDevErrBadSeqlen);
+          continue;
+        }
+        if (it > 0 && !mbar_wait(&bar[PF_QEMPTY], (it - 1) & 1u, wc)) break;
+        const int qrow = ii.b * p.S + ii.s0;
+        mbar_arrive_expect_tx(&bar[PF_QFULL], (uint32_t)kPfQ);
+        tma_load_4d(smem, &tm_qn, &bar[PF_QFULL], 0, qrow, 0, ii.h);
+        tma_load_3d(smem + 2 * kPfAtom, &tm_qr, &bar[PF_QFULL], 0, qrow, ii.h);
+        q_issued = it + 1;
+        const int krow0 = ii.b * p.Lmax;
+        for (int t = 0; t < ii.nt; ++t) {
+          const int krow = krow0 + t * 128;
+          uint32_t st = kc % kPfKStages;
+          if (kc >= (uint32_t)kPfKStages &&
+              !mbar_wait(&bar[PF_KEMPTY + st], ((kc / kPfKStages) - 1) & 1u, wc)) {
+            ok = false;
+            break;
+          }
+          uint8_t* kb = smem + kPfOffK + st * kPfK;
+          mbar_arrive_expect_tx(&bar[PF_KFULL + st], (uint32_t)kPfK);
+          tma_load_4d(kb, &tm_kc, &bar[PF_KFULL + st], 0, krow, 0, ii.h);
+          tma_load_2d(kb + 2 * kPfAtom, &tm_kr, &bar[PF_KFULL + st], 0, krow);
+          ++kc;
+          st = vc % kPfVStages;
+          if (vc >= (uint32_t)kPfVStages &&
+              !mbar_wait(&bar[PF_VEMPTY + st], ((vc / kPfVStages) - 1) & 1u, wc)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&bar[PF_VFULL + st], (uint32_t)kPfV);
+          tma_load_4d(smem + kPfOffV + st * kPfV, &tm_vc, &bar[PF_VFULL + st], 0, krow, 0, ii.h);
+          ++vc;
+        }
+        ++it;
+      }
+      // every copy issued lands before the CTA winds down
+      for (uint32_t j = kc > (uint32_t)kPfKStages ? kc - kPfKStages : 0; j < kc; ++j)
+        mbar_wait_drain(&bar[PF_KFULL + j % kPfKStages], (j / kPfKStages) & 1u, wc);
+      for (uint32_t j = vc > (uint32_t)kPfVStages ? vc - kPfVStages : 0; j < vc; ++j)
+        mbar_wait_drain(&bar[PF_VFULL + j % kPfVStages], (j / kPfVStages) & 1u, wc);
+      if (q_issued > 0) mbar_wait_drain(&bar[PF_QFULL], (q_issued - 1) & 1u, wc);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ MMA issuer
+      constexpr uint32_t idq = idesc_bf16_f32(128, 128, 0, 0);  // S = Q K^T, both K-major
+      constexpr uint32_t idv = idesc_bf16_f32(128, 128, 0, 1);  // O += P V, V MN-major
+      uint32_t kc = 0, vc = 0, g = 0, it = 0;
+      bool ok = true;
+      // QK^T of the tile with running index gg into score buffer gg % 3, whose
+      // previous P (tile gg - 3) must have been consumed by its P.V.
+      auto qk = [&](uint32_t gg) -> bool {
+        const uint32_t sb = gg % 3;
+        if (gg >= 3 && !mbar_wait(&bar[PF_PVDONE + sb], ((gg / 3) - 1) & 1u, wc)) return false;
+        const uint32_t st = kc % kPfKStages;
+        if (!mbar_wait(&bar[PF_KFULL + st], (kc / kPfKStages) & 1u, wc)) return false;
+        tc_fence_after();
+        const uint32_t qa = smem_u32(smem), ka = smem_u32(smem + kPfOffK + st * kPfK);
+#pragma unroll
+        for (int kk = 0; kk < 12; ++kk) {  // 192 = 3 atoms x 4 K-steps of 16
+          const uint32_t off = (uint32_t)((kk >> 2) * kPfAtom + (kk & 3) * 32);
+          mma_ss(tmem + sb * 128, smem_desc(qa + off, 16, 1024, 2), smem_desc(ka + off, 16, 1024, 2), idq,
+                 kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&bar[PF_KEMPTY + st]);
+        mma_commit(&bar[PF_SFULL + sb]);
+        ++kc;
+        return true;
+      };
+      for (int i = blockIdx.x; ok && i < p.n_items; i += gridDim.x) {
+        const PfItem ii = pf_item(p, i);
+        if (!ii.ok) continue;
+        if (!mbar_wait(&bar[PF_QFULL], it & 1u, wc) || !qk(g)) break;
+        for (int t = 0; t < ii.nt; ++t) {
+          if (t + 1 < ii.nt && !qk(g + 1)) {
+            ok = false;
+            break;
+          }
+          if (t + 1 == ii.nt) mma_commit(&bar[PF_QEMPTY]);  // Q is free once these QK^T are done
+          const uint32_t sb = g % 3, st = vc % kPfVStages;
+          if (!mbar_wait(&bar[PF_PREADY + sb], (g / 3) & 1u, wc) ||
+              (t == 0 && it > 0 && !mbar_wait(&bar[PF_OFREE], (it - 1) & 1u, wc)) ||
+              !mbar_wait(&bar[PF_VFULL + st], (vc / kPfVStages) & 1u, wc)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          // tokens any row of the block sees in this tile; rows past them are
+          // weighted 0, but 0 * NaN is not 0, so the rows up to the next
+          // multiple of 16 (one MMA K-step) are zeroed
+          const int nvt = min(128, ii.p_last + 1 - t * 128);
+          const int nk = (nvt + 15) >> 4;
+          uint8_t* vb = smem + kPfOffV + st * kPfV;
+          if (nvt & 15) {
+            for (int a = 0; a < 2; ++a)
+              for (int row = nvt; row < nk * 16; ++row)
+                for (int ch = 0; ch < 8; ++ch)
+                  *reinterpret_cast<uint4*>(vb + a * kPfAtom + row * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
+            fence_proxy_async_cta();
+          }
+          const uint32_t vba = smem_u32(vb);
+          for (int kk = 0; kk < nk; ++kk) {
+            const uint32_t pa = tmem + sb * 128 + (uint32_t)((kk >> 2) * 64 + (kk & 3) * 8);
+            mma_ts(tmem + kPfOCol, pa, smem_desc(vba + (uint32_t)kk * 2048, kPfAtom, 1024, 2), idv,
+                   (t > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(&bar[PF_VEMPTY + st]);
+          mma_commit(&bar[PF_PVDONE + sb]);
+          ++vc;
+          ++g;
+        }
+        ++it;
+      }
+      mma_commit(&bar[PF_DRAIN]);  // every MMA has finished before tensor memory is released
+      mbar_wait_drain(&bar[PF_DRAIN], 0, wc);
+    }
+  } else if (warp >= 4) {
+    // -------------------------------------------------------------- softmax + epilogue
+    const int q4 = warp & 3;
+    const int r = q4 * 32 + lane;  // this thread's row = tensor-memory lane
+    const uint32_t tl = tmem + ((uint32_t)(q4 * 32) << 16);
+    uint32_t g = 0;
+    bool ok = true;
+    for (int i = blockIdx.x; ok && i < p.n_items; i += gridDim.x) {
+      const PfItem ii = pf_item(p, i);
+      if (!ii.ok) continue;
+      const int pr = min(ii.p0 + r, ii.p_last);  // rows past the block's last query repeat it
+      float m_ref = -INFINITY, l = 0.f;
+      for (int t = 0; t < ii.nt; ++t) {
+        const uint32_t sb = g % 3;
+        if (!pf_warp_wait(&bar[PF_SFULL + sb], (g / 3) & 1u, wc)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sc = tl + sb * 128;
+        const int nv = min(max(pr + 1 - t * 128, 0), 128);
+        float mx = -INFINITY;
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+          uint32_t v[16];
+          tmem_ld16(sc + (uint32_t)(c * 16), v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int u = 0; u < 16; ++u)
+            if (c * 16 + u < nv) mx = fmaxf(mx, __uint_as_float(v[u]));
+        }
+        mx *= p.scale_log2;
+        const float cm = ceilf(mx);
+        int ex = 0;  // O and l are rescaled by 2^-ex; 255 stands for 0
+        if (cm > m_ref + 8.f) {
+          ex = (m_ref == -INFINITY) ? 255 : (int)fminf(cm - m_ref, 255.f);
+          l = (ex == 255) ? 0.f : l * pf_exp2_int(-ex);
+          m_ref = cm;
+        }
+        const float mu = (m_ref == -INFINITY) ? 0.f : m_ref;
+        const bool need = t > 0 && ex != 0;
+        if (__any_sync(0xffffffffu, need)) {
+          // O holds this item's earlier tiles once the previous P.V has completed
+          if (!pf_warp_wait(&bar[PF_PVDONE + (g - 1) % 3], ((g - 1) / 3) & 1u, wc)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const float alpha = ex == 255 ? 0.f : pf_exp2_int(-ex);
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            uint32_t v[32];
+            const uint32_t a = tl + kPfOCol + (uint32_t)(c * 32);
+            tmem_ld32(a, v);
+            tmem_wait_ld();
+            if (need) {
+#pragma unroll
+              for (int u = 0; u < 32; ++u) v[u] = __float_as_uint(__uint_as_float(v[u]) * alpha);
+            }
+            tmem_st32(a, v);
+          }
+        }
+        // P = 2^(s scale log2 e - m) in bf16, written over the first 32
+        // columns of each 64-column half once that half has been read
+        float ls = 0.f;
+#pragma unroll 1
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t v[16];
+            tmem_ld16(sc + (uint32_t)(hf * 64 + c * 16), v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const int col = hf * 64 + c * 16 + 2 * u;
+              const float e0 = col < nv ? ex2_approx(fmaf(__uint_as_float(v[2 * u]), p.scale_log2, -mu)) : 0.f;
+              const float e1 =
+                  col + 1 < nv ? ex2_approx(fmaf(__uint_as_float(v[2 * u + 1]), p.scale_log2, -mu)) : 0.f;
+              pk[c * 8 + u] = pack_bf16x2(e0, e1);
+              const __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162*>(&pk[c * 8 + u]);
+              ls += __low2float(b2) + __high2float(b2);
+            }
+          }
+          tmem_st32(sc + (uint32_t)(hf * 64), pk);
+        }
+        tmem_wait_st();
+        l += ls;
+        tc_fence_before();
+        mbar_arrive(&bar[PF_PREADY + sb]);
+        ++g;
+      }
+      if (!ok) break;
+      // epilogue: out = O / l once the item's last P.V has completed
+      if (!pf_warp_wait(&bar[PF_PVDONE + (g - 1) % 3], ((g - 1) / 3) & 1u, wc)) break;
+      tc_fence_after();
+      const float inv = 1.f / l;
+      const bool valid = r < ii.nrow;
+      uint4* orow = reinterpret_cast<uint4*>(p.out + (((size_t)ii.b * p.S + ii.s0 + r) * p.H + ii.h) * 128);
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tl + kPfOCol + (uint32_t)(c * 32), v);
+        tmem_wait_ld();
+        uint32_t o[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u)
+          o[u] = pack_bf16x2(__uint_as_float(v[2 * u]) * inv, __uint_as_float(v[2 * u + 1]) * inv);
+        if (valid) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u) orow[c * 4 + u] = make_uint4(o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&bar[PF_OFREE]);
+    }
+  }
+
+  // ---------------------------------------------------------------- wind down
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace mla

@@ -20,4 +20,6 @@ from .oracle import (  # noqa: F401
     latent_attention,
     output_project,
     fold_output_weights,
+    expand_kv,
+    prefill_attention,
 )

@@ -275,3 +275,46 @@ def fold_output_weights(W_O, W_UV):
     H, d_v, d_c = wv.shape
     assert wo.shape[1] == H * d_v
     return np.concatenate([wo[:, i * d_v:(i + 1) * d_v] @ wv[i] for i in range(H)], axis=1)
+
+
+def expand_kv(c_kv, W):
+    """Keys or values expanded per head ("DeepSeek-V3" (ekkoxiao.github.io),
+    "Multi-Head Latent Attention / KeyValue": k^C_{t,i} = W_i^UK c_t and
+    v^C_{t,i} = W_i^UV c_t).  c_kv [..., d_c], W [H, d, d_c] (fp64, or uint16
+    bf16 bits).  Returns [..., H, d] in fp64: a plain matrix product (numpy)."""
+    cc, ww = _f64(c_kv), _f64(W)
+    H, d, d_c = ww.shape
+    assert cc.shape[-1] == d_c
+    out = cc.reshape(-1, d_c) @ ww.reshape(H * d, d_c).T
+    return out.reshape(*cc.shape[:-1], H, d)
+
+
+def prefill_attention(q_nope, q_rot, k_c, k_rot, v_c, seqlens, *, softmax_scale):
+    """Causal attention over expanded keys and values ("DeepSeek-V3"
+    (ekkoxiao.github.io), "Multi-Head Latent Attention / 注意力计算"): query s of
+    sequence b sits at position t = seqlens[b] - S + s and sees keys 0..t;
+    score_j = (q^C . k^C_j + q^R . k^R_j) * softmax_scale; a = softmax over
+    j <= t (shifted by the row maximum); o = sum_j a_j v^C_j.  q^R and k^R are
+    taken as already rotated.
+      q_nope [B,S,H,d_h], q_rot [B,S,H,d_r], k_c [B,Lmax,H,d_h],
+      k_rot [B,Lmax,d_r], v_c [B,Lmax,H,d_v]  ->  out [B,S,H,d_v] (fp64).
+    Plain numpy products per (sequence, head); cache rows at or past seqlens[b]
+    are never read."""
+    qn, qr, kc, kr, vc = (_f64(a) for a in (q_nope, q_rot, k_c, k_rot, v_c))
+    B, S, H, _ = qn.shape
+    d_v = vc.shape[-1]
+    out = np.empty((B, S, H, d_v), np.float64)
+    for b in range(B):
+        L = int(seqlens[b])
+        assert S <= L <= kc.shape[1]
+        pos = L - S + np.arange(S)
+        visible = np.arange(L)[None, :] <= pos[:, None]          # [S, L]
+        for h in range(H):
+            q = np.concatenate([qn[b, :, h], qr[b, :, h]], axis=1)  # [S, d_h + d_r]
+            k = np.concatenate([kc[b, :L, h], kr[b, :L]], axis=1)   # [L, d_h + d_r]
+            s = (q @ k.T) * softmax_scale
+            s = np.where(visible, s, -np.inf)
+            a = np.exp(s - s.max(axis=1, keepdims=True))
+            a /= a.sum(axis=1, keepdims=True)
+            out[b, :, h] = a @ vc[b, :L, h]
+    return out

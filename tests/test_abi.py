@@ -98,3 +98,19 @@ def test_combine_up_project_host_validation(lib):
 def test_decode_stall_hook_rejects_bad_limits(lib):
     assert lib.mla_debug_decode_stall(ctypes.c_uint64(0)) == 1            # MLA_ERR_INVALID_ARG
     assert lib.mla_debug_decode_stall(ctypes.c_uint64(2_000_000_000)) == 1
+
+
+def test_prefill_host_validation(lib):
+    nul, fake, odd = ctypes.c_void_p(0), ctypes.c_void_p(1 << 20), ctypes.c_void_p((1 << 20) + 2)
+    # expansion: null / misaligned pointers, bad sizes, more than 128 heads
+    assert lib.mla_prefill_expand(nul, fake, fake, fake, fake, 1, 1, 1, None) == 1
+    assert lib.mla_prefill_expand(fake, fake, odd, fake, fake, 1, 1, 1, None) == 1
+    assert lib.mla_prefill_expand(fake, fake, fake, fake, fake, 1, 0, 1, None) == 1
+    assert lib.mla_prefill_expand(fake, fake, fake, fake, fake, 1, 1, 129, None) == 2
+    # attention: nulls, S > Lmax, a non-positive scale, more than 128 heads
+    args = [fake] * 6
+    assert lib.mla_prefill_attention(nul, *args[1:], 1, 1, 1, 1, 0.1, fake, None) == 1
+    assert lib.mla_prefill_attention(*args, 1, 5, 1, 4, 0.1, fake, None) == 1
+    assert lib.mla_prefill_attention(*args, 1, 1, 1, 1, 0.0, fake, None) == 1
+    assert lib.mla_prefill_attention(*args, 1, 1, 1, 1, 0.1, odd, None) == 1
+    assert lib.mla_prefill_attention(*args, 1, 1, 129, 1, 0.1, fake, None) == 2
