@@ -301,9 +301,7 @@ mla_status mla_output_project(const mla_bf16 *x, const mla_bf16 *W, mla_bf16 *u,
  *         length may hold anything, mla_prefill_attention never uses them)
  *   W_UK, W_UV [H,128,512] bf16
  *   k_c, v_c   [B,Lmax,H,128] bf16 outputs
- * Requires 1 <= H <= 128 and B * Lmax <= 4,194,240.  Two launches (one per
- * weight); the weights may stream in before the kernel launched before this
- * call has finished, so they must not be written by that kernel.
+ * Requires 1 <= H <= 128 and B * Lmax < 2^31 - 128.  One launch.
  * Device-side errors go to the library status word.
  */
 mla_status mla_prefill_expand(const mla_bf16 *c_kv, const mla_bf16 *W_UK, const mla_bf16 *W_UV,

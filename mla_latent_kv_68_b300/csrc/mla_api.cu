@@ -17,6 +17,7 @@
 #include "append.cuh"
 #include "combine_up.cuh"
 #include "decode.cuh"
+#include "expand.cuh"
 #include "prefill.cuh"
 #include "rope.cuh"
 #include "splitkv.cuh"
@@ -85,7 +86,9 @@ const DeviceInfo* device_info() {
       cudaFuncSetAttribute(mla::wgemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)mla::wg_smem_bytes(mla::kWgMaxTile)) != cudaSuccess ||
       cudaFuncSetAttribute(mla::prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)mla::kPfSmem) != cudaSuccess)
+                           (int)mla::kPfSmem) != cudaSuccess ||
+      cudaFuncSetAttribute(mla::expand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)mla::kExSmem) != cudaSuccess)
     return nullptr;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -319,7 +322,7 @@ mla_status rope_launch(const mla_bf16* x_in, int64_t in_stride_n, int64_t in_str
     return MLA_ERR_INVALID_ARG;
   if (pos_mode != mla::kPosExplicit && group < 1) return MLA_ERR_INVALID_ARG;
   if (N == 0) return MLA_OK;
-  const long long threads = N * (long long)nh * 8;
+  const long long threads = N * (long long)((nh + mla::kRopeHeads - 1) / mla::kRopeHeads) * 8;
   const int block = 256;
   const long long grid = (threads + block - 1) / block;
   if (grid > 0x7fffffffLL) return MLA_ERR_UNSUPPORTED;
@@ -650,14 +653,14 @@ struct WgPlan {
   size_t ws = 0;
 };
 
-WgPlan wg_plan(int BS, int K, int d, int num_sms, bool split = true) {
+WgPlan wg_plan(int BS, int K, int d, int num_sms) {
   WgPlan w;
   w.n_tile = BS >= mla::kWgMaxTile ? mla::kWgMaxTile : (BS + 15) / 16 * 16;
   w.ntiles = (BS + w.n_tile - 1) / w.n_tile;
   w.mtiles = d / 128;
   w.total_chunks = K / mla::kWgKc;
   const long long tiles = (long long)w.mtiles * w.ntiles;
-  w.ks = split ? (int)std::max(1LL, std::min((long long)w.total_chunks, 2LL * num_sms / std::max(1LL, tiles))) : 1;
+  w.ks = (int)std::max(1LL, std::min((long long)w.total_chunks, 2LL * num_sms / std::max(1LL, tiles)));
   w.ws = w.ks > 1 ? sizeof(float) * (size_t)w.ks * BS * d : 0;
   return w;
 }
@@ -728,16 +731,32 @@ mla_status mla_prefill_expand(const mla_bf16* c_kv, const mla_bf16* W_UK, const 
     return MLA_ERR_INVALID_ARG;
   if (B < 1 || Lmax < 1 || H < 1) return MLA_ERR_INVALID_ARG;
   const long long rows = (long long)B * Lmax;
-  if (H > 128 || rows > 65535LL * mla::kWgMaxTile) return MLA_ERR_UNSUPPORTED;
+  if (H > 128 || rows + 128 > 0x7fffffffLL) return MLA_ERR_UNSUPPORTED;
   const DeviceInfo* dev = device_info();
   if (!dev) return MLA_ERR_CUDA;
-  // k^C[t][h][:] = W_UK[h] c_t: the GEMM u = W x with x = the cache rows
-  // [B*Lmax][512] and W = W_UK seen as [H*128][512]; v^C likewise with W_UV.
-  const int d = H * 128;
-  const WgPlan w = wg_plan((int)rows, MLA_D_C, d, dev->num_sms, false);
-  const mla_status s1 = wg_launch(c_kv, W_UK, k_c, (int)rows, MLA_D_C, d, w, dev, nullptr, stream);
-  if (s1 != MLA_OK) return s1;
-  return wg_launch(c_kv, W_UV, v_c, (int)rows, MLA_D_C, d, w, dev, nullptr, stream);
+  // [rows][512] seen as [64 columns][rows][8 atoms]: the latent rows in two
+  // boxes of four atoms (64 KB), a weight's 128 rows of one head in boxes of
+  // two atoms (32 KB)
+  const cuuint64_t str[2] = {1024, 128};
+  const cuuint64_t dc[3] = {64, (cuuint64_t)rows, 8}, dw[3] = {64, (cuuint64_t)H * 128, 8};
+  const cuuint32_t bc[3] = {64, 128, 4}, bw[3] = {64, 128, 2};
+  CUtensorMap tc, tk, tv;
+  if (!encode_tiled(&tc, c_kv, 3, dc, str, bc) || !encode_tiled(&tk, W_UK, 3, dw, str, bw) ||
+      !encode_tiled(&tv, W_UV, 3, dw, str, bw))
+    return MLA_ERR_INVALID_ARG;
+  mla::ExpandParams p;
+  p.k_c = reinterpret_cast<__nv_bfloat16*>(k_c);
+  p.v_c = reinterpret_cast<__nv_bfloat16*>(v_c);
+  p.T = (int)rows;
+  p.H = H;
+  p.n_tt = (int)((rows + 127) / 128);
+  p.n_grp = 2 * ((H + mla::kExGroup - 1) / mla::kExGroup);
+  p.status = dev->kernel_status;
+  p.timeout_ns = kTimeoutNs;
+  const long long units = (long long)p.n_tt * p.n_grp;
+  const int grid = (int)std::min<long long>(units, dev->num_sms);
+  return launch_ex(mla::expand_kernel, dim3((unsigned)grid), dim3(mla::kExThreads), mla::kExSmem,
+                   (cudaStream_t)stream, true, 1, tc, tk, tv, p);
 }
 
 mla_status mla_prefill_attention(const mla_bf16* q_nope, const mla_bf16* q_rope, const mla_bf16* k_c,
@@ -776,11 +795,11 @@ mla_status mla_prefill_attention(const mla_bf16* q_nope, const mla_bf16* q_rope,
   p.H = H;
   p.Lmax = Lmax;
   p.nq = nq;
-  p.n_items = B * H * nq;
+  p.n_units = B * H * ((nq + 1) / 2);
   p.scale_log2 = (float)((double)softmax_scale * 1.4426950408889634);
   p.status = dev->kernel_status;
   p.timeout_ns = kTimeoutNs;
-  const int grid = std::min(p.n_items, dev->num_sms);
+  const int grid = std::min(p.n_units, dev->num_sms);
   return launch_ex(mla::prefill_kernel, dim3((unsigned)grid), dim3(mla::kPfThreads), mla::kPfSmem,
                    (cudaStream_t)stream, true, 1, tqn, tqr, tkc, tkr, tvc, p);
 }

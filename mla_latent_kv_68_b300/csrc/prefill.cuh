@@ -12,10 +12,12 @@
 //
 // A work item is 128 consecutive query positions of one (sequence, head); its
 // rows see keys 0 .. their own position, so the item walks key tiles of 128
-// from the start of the sequence to the tile holding its last position.  One
-// persistent CTA per SM takes items round-robin (heaviest first within each
-// head, and the items of one head next to each other, so that a head's
-// expanded keys and values are read from HBM about once and then from L2).
+// from the start of the sequence to the tile holding its last position.  A
+// unit pairs a head's last query block with its first, its second last with
+// its second, and so on, so that the units of a sequence cost the same; one
+// persistent CTA per SM takes units round-robin, head after head, so that the
+// CTAs work on a few heads at a time and a head's expanded keys and values
+// are read from HBM about once and then from L2.
 //
 // Per CTA (256 threads): warp 0 issues TMA copies (Q once per item: q^C and
 // q^R as three 128-byte-swizzle atoms; per key tile: k^C, k^R, v^C), warp 1
@@ -55,7 +57,7 @@ struct PrefillParams {
   const int32_t* seqlens;    // [B]: cached tokens, the S new ones included
   int B, S, H, Lmax;
   int nq;                    // query blocks of 128 per (sequence, head)
-  int n_items;               // B * H * nq
+  int n_units;               // B * H * ceil(nq / 2)
   float scale_log2;          // softmax scale * log2(e)
   uint32_t* status;
   uint64_t timeout_ns;
@@ -66,12 +68,22 @@ struct PfItem {
   bool ok;
 };
 
-// Item i: head-major (b, h), and within a head the query blocks from the last
-// (the most key tiles) to the first.
-__device__ __forceinline__ PfItem pf_item(const PrefillParams& p, int i) {
+// Work unit u of (sequence, head) bh = u / np: query blocks nq - 1 - k and k
+// (k = u mod np, np = ceil(nq / 2); one block when they coincide), so that
+// every unit of a sequence walks the same number of key tiles and the CTAs,
+// taking units round-robin, stay on the same few heads (whose expanded keys
+// and values then come from L2).
+__device__ __forceinline__ int pf_unit_blocks(const PrefillParams& p, int u, int (&qb)[2], int& bh) {
+  const int np = (p.nq + 1) >> 1;
+  bh = u / np;
+  const int k = u - bh * np;
+  qb[0] = p.nq - 1 - k;
+  qb[1] = k;
+  return qb[0] == k ? 1 : 2;
+}
+
+__device__ __forceinline__ PfItem pf_item(const PrefillParams& p, int bh, int qb) {
   PfItem it;
-  const int bh = i / p.nq;
-  const int qb = p.nq - 1 - (i - bh * p.nq);
   it.b = bh / p.H;
   it.h = bh - it.b * p.H;
   const int L = __ldg(p.seqlens + it.b);
@@ -83,6 +95,25 @@ __device__ __forceinline__ PfItem pf_item(const PrefillParams& p, int i) {
   it.nt = it.ok ? it.p_last / 128 + 1 : 0;
   return it;
 }
+
+// This CTA's items in order: units blockIdx.x, blockIdx.x + gridDim.x, ...,
+// each one or two query blocks.
+struct PfIter {
+  int u = (int)blockIdx.x, slot = 0;
+  __device__ __forceinline__ bool next(const PrefillParams& p, PfItem& it) {
+    while (u < p.n_units) {
+      int qb[2], bh;
+      const int n = pf_unit_blocks(p, u, qb, bh);
+      if (slot < n) {
+        it = pf_item(p, bh, qb[slot++]);
+        return true;
+      }
+      u += (int)gridDim.x;
+      slot = 0;
+    }
+    return false;
+  }
+};
 
 __device__ __forceinline__ bool pf_warp_wait(uint64_t* bar, uint32_t parity, const WaitCtx& w) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, w));
@@ -133,8 +164,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       // ------------------------------------------------------------ TMA producer
       uint32_t kc = 0, vc = 0, it = 0, q_issued = 0;
       bool ok = true;
-      for (int i = blockIdx.x; ok && i < p.n_items; i += gridDim.x) {
-        const PfItem ii = pf_item(p, i);
+      PfIter iter;
+      PfItem ii;
+      while (ok && iter.next(p, ii)) {
         if (!ii.ok) {
           atomicOr(p.status, kDevErrBadSeqlen);
           continue;
@@ -205,8 +237,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         ++kc;
         return true;
       };
-      for (int i = blockIdx.x; ok && i < p.n_items; i += gridDim.x) {
-        const PfItem ii = pf_item(p, i);
+      PfIter iter;
+      PfItem ii;
+      while (ok && iter.next(p, ii)) {
         if (!ii.ok) continue;
         if (!mbar_wait(&bar[PF_QFULL], it & 1u, wc) || !qk(g)) break;
         for (int t = 0; t < ii.nt; ++t) {
@@ -259,8 +292,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const uint32_t tl = tmem + ((uint32_t)(q4 * 32) << 16);
     uint32_t g = 0;
     bool ok = true;
-    for (int i = blockIdx.x; ok && i < p.n_items; i += gridDim.x) {
-      const PfItem ii = pf_item(p, i);
+    PfIter iter;
+    PfItem ii;
+    while (ok && iter.next(p, ii)) {
       if (!ii.ok) continue;
       const int pr = min(ii.p0 + r, ii.p_last);  // rows past the block's last query repeat it
       float m_ref = -INFINITY, l = 0.f;
@@ -273,16 +307,25 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         tc_fence_after();
         const uint32_t sc = tl + sb * 128;
         const int nv = min(max(pr + 1 - t * 128, 0), 128);
-        float mx = -INFINITY;
-#pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
-          uint32_t v[16];
-          tmem_ld16(sc + (uint32_t)(c * 16), v);
-          tmem_wait_ld();
+        // the row's 128 scores, read from tensor memory once
+        uint32_t v[128];
 #pragma unroll
-          for (int u = 0; u < 16; ++u)
-            if (c * 16 + u < nv) mx = fmaxf(mx, __uint_as_float(v[u]));
+        for (int c = 0; c < 4; ++c) tmem_ld32(sc + (uint32_t)(c * 32), *reinterpret_cast<uint32_t(*)[32]>(&v[c * 32]));
+        tmem_wait_ld();
+        const bool full = __all_sync(0xffffffffu, nv == 128);  // no column of this warp's rows is masked
+        // row maximum over eight independent partial maxima (short dependency chains)
+        float pm[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) pm[k] = -INFINITY;
+        if (full) {
+#pragma unroll
+          for (int u = 0; u < 128; ++u) pm[u & 7] = fmaxf(pm[u & 7], __uint_as_float(v[u]));
+        } else {
+#pragma unroll
+          for (int u = 0; u < 128; ++u)
+            if (u < nv) pm[u & 7] = fmaxf(pm[u & 7], __uint_as_float(v[u]));
         }
+        float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])), fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
         mx *= p.scale_log2;
         const float cm = ceilf(mx);
         int ex = 0;  // O and l are rescaled by 2^-ex; 255 stands for 0
@@ -303,41 +346,42 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           const float alpha = ex == 255 ? 0.f : pf_exp2_int(-ex);
 #pragma unroll 1
           for (int c = 0; c < 4; ++c) {
-            uint32_t v[32];
+            uint32_t o[32];
             const uint32_t a = tl + kPfOCol + (uint32_t)(c * 32);
-            tmem_ld32(a, v);
+            tmem_ld32(a, o);
             tmem_wait_ld();
             if (need) {
 #pragma unroll
-              for (int u = 0; u < 32; ++u) v[u] = __float_as_uint(__uint_as_float(v[u]) * alpha);
+              for (int u = 0; u < 32; ++u) o[u] = __float_as_uint(__uint_as_float(o[u]) * alpha);
             }
-            tmem_st32(a, v);
+            tmem_st32(a, o);
           }
         }
         // P = 2^(s scale log2 e - m) in bf16, written over the first 32
-        // columns of each 64-column half once that half has been read
-        float ls = 0.f;
-#pragma unroll 1
+        // columns of each 64-column half (already read above)
+        float lsa[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) lsa[k] = 0.f;
+#pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
           uint32_t pk[32];
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t v[16];
-            tmem_ld16(sc + (uint32_t)(hf * 64 + c * 16), v);
-            tmem_wait_ld();
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              const int col = hf * 64 + c * 16 + 2 * u;
-              const float e0 = col < nv ? ex2_approx(fmaf(__uint_as_float(v[2 * u]), p.scale_log2, -mu)) : 0.f;
-              const float e1 =
-                  col + 1 < nv ? ex2_approx(fmaf(__uint_as_float(v[2 * u + 1]), p.scale_log2, -mu)) : 0.f;
-              pk[c * 8 + u] = pack_bf16x2(e0, e1);
-              const __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162*>(&pk[c * 8 + u]);
-              ls += __low2float(b2) + __high2float(b2);
+          for (int u = 0; u < 32; ++u) {
+            const int col = hf * 64 + 2 * u;
+            float e0 = ex2_approx(fmaf(__uint_as_float(v[col]), p.scale_log2, -mu));
+            float e1 = ex2_approx(fmaf(__uint_as_float(v[col + 1]), p.scale_log2, -mu));
+            if (!full) {
+              e0 = col < nv ? e0 : 0.f;
+              e1 = col + 1 < nv ? e1 : 0.f;
             }
+            pk[u] = pack_bf16x2(e0, e1);
+            // the row sum adds exactly the bf16 weights that P.V multiplies
+            lsa[(2 * u) & 7] += __uint_as_float(pk[u] << 16);
+            lsa[(2 * u + 1) & 7] += __uint_as_float(pk[u] & 0xffff0000u);
           }
           tmem_st32(sc + (uint32_t)(hf * 64), pk);
         }
+        const float ls = ((lsa[0] + lsa[1]) + (lsa[2] + lsa[3])) + ((lsa[4] + lsa[5]) + (lsa[6] + lsa[7]));
         tmem_wait_st();
         l += ls;
         tc_fence_before();

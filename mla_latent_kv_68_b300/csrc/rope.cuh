@@ -7,7 +7,8 @@
 // "Multi-Head Latent Attention / KeyValue" applies it to the shared key k^R at
 // the key's own position, "Query" to every head's q^R at the query position.
 //
-// One thread rotates 4 pairs (16 bytes).  The angle m * theta_j is formed and
+// One thread rotates 4 pairs (16 bytes) of every head of a row in turn (up
+// to 16 heads).  The angle m * theta_j is formed and
 // reduced modulo 2 pi in fp64 (positions reach 2^17 and beyond, where an fp32
 // product would already be off by ~1e-2 rad); sin/cos of the reduced angle and
 // the rotation itself are fp32; the result is rounded to bf16.
@@ -48,6 +49,36 @@ __device__ __forceinline__ uint4 rope_rotate4(uint4 v, int64_t pos, int part, co
 }
 
 
+// cos and sin of the angles of pairs part*4 .. part*4+3 at position `pos`
+// (the angle reduced modulo 2 pi in fp64, as in rope_rotate4).
+__device__ __forceinline__ void rope_angles4(int64_t pos, int part, const RopeTheta& th, float (&cs)[4],
+                                             float (&sn)[4]) {
+  const double two_pi = 6.283185307179586476925286766559;
+  const double inv_two_pi = 0.15915494309189533576888376337251;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const double a = (double)pos * th.theta[part * 4 + k];
+    const double r = fma(-rint(a * inv_two_pi), two_pi, a);
+    sincosf((float)r, &sn[k], &cs[k]);
+  }
+}
+
+__device__ __forceinline__ uint4 rope_turn4(uint4 v, const float (&cs)[4], const float (&sn)[4]) {
+  uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    __nv_bfloat162 pr = *reinterpret_cast<__nv_bfloat162*>(&w[k]);
+    const float x = __low2float(pr), y = __high2float(pr);
+    __nv_bfloat162 o = __floats2bfloat162_rn(x * cs[k] - y * sn[k], x * sn[k] + y * cs[k]);
+    w[k] = *reinterpret_cast<uint32_t*>(&o);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+constexpr int kRopeHeads = 16;  // heads per thread: the angles are formed once for all of them
+
+// One thread: 4 pairs (16 bytes) of row n for up to kRopeHeads heads, which
+// share the row's position and hence its angles.
 __global__ void __launch_bounds__(256) rope_kernel(const __nv_bfloat16* __restrict__ x_in,
                                                    int64_t in_sn, int64_t in_sh,
                                                    __nv_bfloat16* __restrict__ x_out,
@@ -55,13 +86,13 @@ __global__ void __launch_bounds__(256) rope_kernel(const __nv_bfloat16* __restri
                                                    int nh, int pos_mode,
                                                    const int32_t* __restrict__ pos_src, int group,
                                                    const RopeTheta th) {
+  const int nhc = (nh + kRopeHeads - 1) / kRopeHeads;
   const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  const int64_t total = N * nh * 8;  // 8 threads per 64-element row
-  if (tid >= total) return;
+  if (tid >= N * nhc * 8) return;
   const int part = (int)(tid & 7);
-  const int64_t rh = tid >> 3;
-  const int64_t n = rh / nh;
-  const int hd = (int)(rh - n * nh);
+  const int64_t rc = tid >> 3;
+  const int64_t n = rc / nhc;
+  const int hc = (int)(rc - n * nhc);
 
   int64_t pos;
   if (pos_mode == kPosExplicit) {
@@ -78,8 +109,13 @@ __global__ void __launch_bounds__(256) rope_kernel(const __nv_bfloat16* __restri
     pos = j;
   }
 
-  const uint4 v = *reinterpret_cast<const uint4*>(x_in + n * in_sn + hd * in_sh + part * 8);
-  *reinterpret_cast<uint4*>(x_out + n * out_sn + hd * out_sh + part * 8) = rope_rotate4(v, pos, part, th);
+  float cs[4], sn[4];
+  rope_angles4(pos, part, th, cs, sn);
+  const int h1 = min(nh, (hc + 1) * kRopeHeads);
+  for (int hd = hc * kRopeHeads; hd < h1; ++hd) {
+    const uint4 v = *reinterpret_cast<const uint4*>(x_in + n * in_sn + hd * in_sh + part * 8);
+    *reinterpret_cast<uint4*>(x_out + n * out_sn + hd * out_sh + part * 8) = rope_turn4(v, cs, sn);
+  }
 }
 
 }  // namespace mla
