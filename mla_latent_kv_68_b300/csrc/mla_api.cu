@@ -46,6 +46,9 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 #ifdef MLA_DECODE_TRACE
 unsigned long long* g_decode_trace = nullptr;  // diagnostic build only: timeline buffer
 #endif
+#ifdef MLA_PREFILL_TRACE
+unsigned long long* g_prefill_trace = nullptr;  // diagnostic build only: timeline buffer
+#endif
 
 // Test hook (mla_debug_decode_stall): the wait limit of the next mla_decode
 // call whose plan barrier is left incomplete; 0 = none pending.
@@ -238,6 +241,14 @@ const char* mla_status_string(int s) {
 }
 
 int mla_version(void) { return 100; }
+
+#ifdef MLA_PREFILL_TRACE
+// Diagnostic build only: device buffer of 8-byte stamps [8][8][128], filled by
+// later mla_prefill_attention calls.
+void mla_debug_set_prefill_trace(void* device_buffer) {
+  g_prefill_trace = static_cast<unsigned long long*>(device_buffer);
+}
+#endif
 
 #ifdef MLA_DECODE_TRACE
 // Diagnostic build only: device buffer of 8-byte stamps,
@@ -799,6 +810,11 @@ mla_status mla_prefill_attention(const mla_bf16* q_nope, const mla_bf16* q_rope,
   p.scale_log2 = (float)((double)softmax_scale * 1.4426950408889634);
   p.status = dev->kernel_status;
   p.timeout_ns = kTimeoutNs;
+#ifdef MLA_PREFILL_TRACE
+  p.trace = g_prefill_trace;
+#else
+  p.trace = nullptr;
+#endif
   const int grid = std::min(p.n_units, dev->num_sms);
   return launch_ex(mla::prefill_kernel, dim3((unsigned)grid), dim3(mla::kPfThreads), mla::kPfSmem,
                    (cudaStream_t)stream, true, 1, tqn, tqr, tkc, tkr, tvc, p);

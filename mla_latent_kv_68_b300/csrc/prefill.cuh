@@ -19,10 +19,11 @@
 // CTAs work on a few heads at a time and a head's expanded keys and values
 // are read from HBM about once and then from L2.
 //
-// Per CTA (256 threads): warp 0 issues TMA copies (Q once per item: q^C and
-// q^R as three 128-byte-swizzle atoms; per key tile: k^C, k^R, v^C), warp 1
-// issues the MMAs (one thread), warps 4..7 run the online softmax, one row per
-// thread, and the epilogue; warps 2..3 only take part in set-up and wind-down.
+// Per CTA (256 threads): warp 0 issues the TMA copies of Q (once per item:
+// q^C and q^R as three 128-byte-swizzle atoms) and of each key tile (k^C,
+// k^R), warp 2 those of each value tile (v^C), warp 1 issues the MMAs (one
+// thread), warps 4..7 run the online softmax, one row per thread, and the
+// epilogue; warp 3 only takes part in set-up and wind-down.
 // Tensor memory holds three 128-column score buffers S and the 128 x 128 fp32
 // output O (columns 384..511).  QK^T of tile t + 1 runs while the softmax
 // works on tile t; the softmax writes P (bf16) over the first half of each
@@ -42,6 +43,7 @@ constexpr int kPfQ = 3 * kPfAtom;   // q^C (two atoms) + q^R (one)
 constexpr int kPfK = 3 * kPfAtom;   // k^C (two atoms) + k^R (one)
 constexpr int kPfV = 2 * kPfAtom;   // v^C (two atoms)
 constexpr int kPfKStages = 2, kPfVStages = 2;
+static_assert(kPfKStages == 2 && kPfVStages == 2, "the producers index two-deep rings");
 constexpr int kPfOffK = kPfQ;
 constexpr int kPfOffV = kPfOffK + kPfKStages * kPfK;
 constexpr int kPfOffBar = kPfOffV + kPfVStages * kPfV;
@@ -61,7 +63,24 @@ struct PrefillParams {
   float scale_log2;          // softmax scale * log2(e)
   uint32_t* status;
   uint64_t timeout_ns;
+  unsigned long long* trace;  // timeline of a diagnostic build (MLA_PREFILL_TRACE), else unused
 };
+
+// Diagnostic timeline: with MLA_PREFILL_TRACE defined, CTAs 0..7 stamp
+// %globaltimer at events of their first 128 key tiles into
+// trace[cta][event][tile].  Compiled out otherwise.
+enum : int { PT_KFULL = 0, PT_QK = 1, PT_SREADY = 2, PT_PREADY = 3, PT_PSEEN = 4, PT_VFULL = 5, PT_PV = 6, PT_NEV = 8 };
+#ifdef MLA_PREFILL_TRACE
+#define PF_TRACE(p, ev, g)                                                                   \
+  do {                                                                                       \
+    if ((p).trace && blockIdx.x < 8 && (g) < 128)                                            \
+      (p).trace[((size_t)blockIdx.x * PT_NEV + (ev)) * 128 + (g)] = global_timer_ns();       \
+  } while (0)
+#else
+#define PF_TRACE(p, ev, g) \
+  do {                     \
+  } while (0)
+#endif
 
 struct PfItem {
   int b, h, s0, nrow, p0, p_last, nt;
@@ -159,55 +178,52 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   pdl_trigger();
   pdl_wait();  // q, the expanded keys and values and the cache come from earlier kernels
 
-  if (warp == 0) {
+  if (warp == 0 || warp == 2) {
     if (lane == 0) {
-      // ------------------------------------------------------------ TMA producer
-      uint32_t kc = 0, vc = 0, it = 0, q_issued = 0;
+      // -------------------------------------------------- TMA producers: warp 0
+      // loads Q and the key tiles, warp 2 the value tiles, each on its own ring
+      // so that neither waits for the other's slots
+      const bool keys = warp == 0;
+      uint32_t c = 0, it = 0, q_issued = 0;
       bool ok = true;
       PfIter iter;
       PfItem ii;
       while (ok && iter.next(p, ii)) {
         if (!ii.ok) {
-          atomicOr(p.status, kDevErrBadSeqlen);
+          if (keys) atomicOr(p.status, kDevErrBadSeqlen);
           continue;
         }
-        if (it > 0 && !mbar_wait(&bar[PF_QEMPTY], (it - 1) & 1u, wc)) break;
-        const int qrow = ii.b * p.S + ii.s0;
-        mbar_arrive_expect_tx(&bar[PF_QFULL], (uint32_t)kPfQ);
-        tma_load_4d(smem, &tm_qn, &bar[PF_QFULL], 0, qrow, 0, ii.h);
-        tma_load_3d(smem + 2 * kPfAtom, &tm_qr, &bar[PF_QFULL], 0, qrow, ii.h);
-        q_issued = it + 1;
+        if (keys) {
+          if (it > 0 && !mbar_wait(&bar[PF_QEMPTY], (it - 1) & 1u, wc)) break;
+          const int qrow = ii.b * p.S + ii.s0;
+          mbar_arrive_expect_tx(&bar[PF_QFULL], (uint32_t)kPfQ);
+          tma_load_4d(smem, &tm_qn, &bar[PF_QFULL], 0, qrow, 0, ii.h);
+          tma_load_3d(smem + 2 * kPfAtom, &tm_qr, &bar[PF_QFULL], 0, qrow, ii.h);
+          q_issued = it + 1;
+        }
         const int krow0 = ii.b * p.Lmax;
-        for (int t = 0; t < ii.nt; ++t) {
+        for (int t = 0; t < ii.nt; ++t, ++c) {
           const int krow = krow0 + t * 128;
-          uint32_t st = kc % kPfKStages;
-          if (kc >= (uint32_t)kPfKStages &&
-              !mbar_wait(&bar[PF_KEMPTY + st], ((kc / kPfKStages) - 1) & 1u, wc)) {
+          const uint32_t st = c % 2;  // both rings are two deep
+          if (c >= 2 && !mbar_wait(&bar[(keys ? PF_KEMPTY : PF_VEMPTY) + st], ((c / 2) - 1) & 1u, wc)) {
             ok = false;
             break;
           }
-          uint8_t* kb = smem + kPfOffK + st * kPfK;
-          mbar_arrive_expect_tx(&bar[PF_KFULL + st], (uint32_t)kPfK);
-          tma_load_4d(kb, &tm_kc, &bar[PF_KFULL + st], 0, krow, 0, ii.h);
-          tma_load_2d(kb + 2 * kPfAtom, &tm_kr, &bar[PF_KFULL + st], 0, krow);
-          ++kc;
-          st = vc % kPfVStages;
-          if (vc >= (uint32_t)kPfVStages &&
-              !mbar_wait(&bar[PF_VEMPTY + st], ((vc / kPfVStages) - 1) & 1u, wc)) {
-            ok = false;
-            break;
+          if (keys) {
+            uint8_t* kb = smem + kPfOffK + st * kPfK;
+            mbar_arrive_expect_tx(&bar[PF_KFULL + st], (uint32_t)kPfK);
+            tma_load_4d(kb, &tm_kc, &bar[PF_KFULL + st], 0, krow, 0, ii.h);
+            tma_load_2d(kb + 2 * kPfAtom, &tm_kr, &bar[PF_KFULL + st], 0, krow);
+          } else {
+            mbar_arrive_expect_tx(&bar[PF_VFULL + st], (uint32_t)kPfV);
+            tma_load_4d(smem + kPfOffV + st * kPfV, &tm_vc, &bar[PF_VFULL + st], 0, krow, 0, ii.h);
           }
-          mbar_arrive_expect_tx(&bar[PF_VFULL + st], (uint32_t)kPfV);
-          tma_load_4d(smem + kPfOffV + st * kPfV, &tm_vc, &bar[PF_VFULL + st], 0, krow, 0, ii.h);
-          ++vc;
         }
         ++it;
       }
       // every copy issued lands before the CTA winds down
-      for (uint32_t j = kc > (uint32_t)kPfKStages ? kc - kPfKStages : 0; j < kc; ++j)
-        mbar_wait_drain(&bar[PF_KFULL + j % kPfKStages], (j / kPfKStages) & 1u, wc);
-      for (uint32_t j = vc > (uint32_t)kPfVStages ? vc - kPfVStages : 0; j < vc; ++j)
-        mbar_wait_drain(&bar[PF_VFULL + j % kPfVStages], (j / kPfVStages) & 1u, wc);
+      const int full = keys ? PF_KFULL : PF_VFULL;
+      for (uint32_t j = c > 2u ? c - 2 : 0; j < c; ++j) mbar_wait_drain(&bar[full + j % 2], (j / 2) & 1u, wc);
       if (q_issued > 0) mbar_wait_drain(&bar[PF_QFULL], (q_issued - 1) & 1u, wc);
     }
   } else if (warp == 1) {
@@ -224,6 +240,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         if (gg >= 3 && !mbar_wait(&bar[PF_PVDONE + sb], ((gg / 3) - 1) & 1u, wc)) return false;
         const uint32_t st = kc % kPfKStages;
         if (!mbar_wait(&bar[PF_KFULL + st], (kc / kPfKStages) & 1u, wc)) return false;
+        PF_TRACE(p, PT_KFULL, gg);
         tc_fence_after();
         const uint32_t qa = smem_u32(smem), ka = smem_u32(smem + kPfOffK + st * kPfK);
 #pragma unroll
@@ -234,6 +251,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
         mma_commit(&bar[PF_KEMPTY + st]);
         mma_commit(&bar[PF_SFULL + sb]);
+        PF_TRACE(p, PT_QK, gg);
         ++kc;
         return true;
       };
@@ -250,11 +268,16 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           if (t + 1 == ii.nt) mma_commit(&bar[PF_QEMPTY]);  // Q is free once these QK^T are done
           const uint32_t sb = g % 3, st = vc % kPfVStages;
           if (!mbar_wait(&bar[PF_PREADY + sb], (g / 3) & 1u, wc) ||
-              (t == 0 && it > 0 && !mbar_wait(&bar[PF_OFREE], (it - 1) & 1u, wc)) ||
-              !mbar_wait(&bar[PF_VFULL + st], (vc / kPfVStages) & 1u, wc)) {
+              (t == 0 && it > 0 && !mbar_wait(&bar[PF_OFREE], (it - 1) & 1u, wc))) {
             ok = false;
             break;
           }
+          PF_TRACE(p, PT_PSEEN, g);
+          if (!mbar_wait(&bar[PF_VFULL + st], (vc / kPfVStages) & 1u, wc)) {
+            ok = false;
+            break;
+          }
+          PF_TRACE(p, PT_VFULL, g);
           tc_fence_after();
           // tokens any row of the block sees in this tile; rows past them are
           // weighted 0, but 0 * NaN is not 0, so the rows up to the next
@@ -277,6 +300,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           }
           mma_commit(&bar[PF_VEMPTY + st]);
           mma_commit(&bar[PF_PVDONE + sb]);
+          PF_TRACE(p, PT_PV, g);
           ++vc;
           ++g;
         }
@@ -304,6 +328,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           ok = false;
           break;
         }
+        if (r == 0) PF_TRACE(p, PT_SREADY, g);
         tc_fence_after();
         const uint32_t sc = tl + sb * 128;
         const int nv = min(max(pr + 1 - t * 128, 0), 128);
@@ -386,6 +411,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         l += ls;
         tc_fence_before();
         mbar_arrive(&bar[PF_PREADY + sb]);
+        if (r == 0) PF_TRACE(p, PT_PREADY, g);
         ++g;
       }
       if (!ok) break;
