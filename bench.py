@@ -397,7 +397,7 @@ def _time_output_project(args, x, dev, stream, flush_l2, mb):
 PREFILL = dict(name="prefill_b4_s4096_h128", B=4, S=4096, H=128)
 
 
-def _time_prefill(args, dev, stream, flush_l2, mb):
+def _time_prefill(args, dev, stream, flush_l2, mb, batch=None):
     """Prefill of whole prompts (not part of the decode step): B prompts of S
     tokens, every position querying the cache up to itself.  Times the three
     phases (RoPE of the queries, expansion of keys and values per head, causal
@@ -405,7 +405,7 @@ def _time_prefill(args, dev, stream, flush_l2, mb):
     L2 flush.  Algorithmic flops: 2 x 2 x (B S) x (H 128) x 512 for the
     expansion and 2 x (192 + 128) x H per visible (query, key) pair."""
     from mla_latent_kv_68_b300.inputs import make_inputs
-    B, S, H = PREFILL["B"], PREFILL["S"], PREFILL["H"]
+    B, S, H = batch or PREFILL["B"], PREFILL["S"], PREFILL["H"]
     x = make_inputs(B, S, H, [S] * B, seed=68005)
     d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
     mb.rope_cache(d["k_r"], d["seqlens"])
@@ -441,14 +441,15 @@ def _time_prefill(args, dev, stream, flush_l2, mb):
     del graphs, step, d, x
     torch.cuda.empty_cache()
     total_us, attn_us = times
-    return {"workload": f"{PREFILL['name']}: {B} prompts of {S} tokens, {H} heads, causal",
+    name = PREFILL["name"] if B == PREFILL["B"] else f"prefill_b{B}_s{S}_h{H}"
+    return {"workload": f"{name}: {B} prompts of {S} tokens, {H} heads, causal",
             "us": round(total_us, 3), "attention_us": round(attn_us, 3),
             "flops": f_attn + f_exp, "attention_flops": f_attn,
             "tflops": round((f_attn + f_exp) / (total_us * 1e-6) / 1e12, 1),
             "attention_tflops": round(f_attn / (attn_us * 1e-6) / 1e12, 1),
             "frac": round((f_attn + f_exp) / (total_us * 1e-6) / 1e12 / tf_burst, 4),
             "attention_frac": round(f_attn / (attn_us * 1e-6) / 1e12 / tf_burst, 4),
-            "peak_tflops": tf_burst, "launches": 4}
+            "peak_tflops": tf_burst, "launches": 3}
 
 
 def run_ours(args, rank, world, local_rank):
@@ -570,9 +571,21 @@ def main(argv=None):
     ap.add_argument("--ref-seconds", type=float, default=12.0)
     ap.add_argument("--rope", default="plain", choices=["plain", "yarn"],
                     help="RoPE frequencies of the step (yarn: the long-context setting)")
+    ap.add_argument("--prefill-only", action="store_true",
+                    help="measure only the prefill (its JSON object), for profiling")
+    ap.add_argument("--prefill-batch", type=int, default=PREFILL["B"],
+                    help="prompts of the prefill workload (4096 tokens each)")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be >= 3")
+    if args.prefill_only:
+        from mla_latent_kv_68_b300 import binding as mb
+        dev = torch.device("cuda", 0)
+        mb.lib()
+        flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        print(json.dumps(_time_prefill(args, dev, torch.cuda.current_stream(dev), flush.zero_, mb,
+                                       batch=args.prefill_batch)), flush=True)
+        return 0
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
