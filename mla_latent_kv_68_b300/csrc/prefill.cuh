@@ -19,21 +19,17 @@
 // CTAs work on a few heads at a time and a head's expanded keys and values
 // are read from HBM about once and then from L2.
 //
-// Per CTA (256 threads): warp 0 issues the TMA copies of each item's Q (q^C
-// and q^R, three 128-byte-swizzle atoms) and key tiles (k^C, k^R) through one
-// ring of three 48 KB stages, warp 2 those of the value tiles (v^C) through a
-// ring of two 32 KB stages; warp 1 issues the MMAs (one thread); warps 4..7
-// run the online softmax, one row per thread, and the epilogue; warp 3 only
-// takes part in set-up and wind-down.  The MMA thread copies Q from its stage
-// into tensor memory (tcgen05.cp), so QK^T reads only K from shared memory;
-// the next item's Q streams in behind the current item's last key tiles.
-// Tensor memory holds two 128-column score buffers S, the 128 x 128 fp32
-// output O and Q (96 columns).  QK^T of tile t + 1 runs while the softmax works
-// on tile t; the softmax writes P (bf16) over the first half of each 64-column
-// half of its S buffer and P.V reads it from there (A operand in tensor
-// memory).  The online softmax keeps an integer reference exponent per row
-// (log2 units) that moves only when a tile's maximum passes it by more than
-// 8, so every rescale of O and of the row sum is an exact power of two.
+// Per CTA (256 threads): warp 0 issues the TMA copies of Q (once per item:
+// q^C and q^R as three 128-byte-swizzle atoms) and of each key tile (k^C,
+// k^R), warp 2 those of each value tile (v^C), warp 1 issues the MMAs (one
+// thread), warps 4..7 run the online softmax, one row per thread, and the
+// epilogue; warp 3 only takes part in set-up and wind-down.
+// Tensor memory holds three 128-column score buffers S and the 128 x 128 fp32
+// output O (columns 384..511).  QK^T runs two tiles ahead of the softmax; the softmax writes P (bf16) over the first half of each
+// 64-column half of its S buffer and P.V reads it from there (A operand in
+// tensor memory).  The online softmax keeps an integer reference exponent per
+// row (log2 units) that moves only when a tile's maximum passes it by more
+// than 8, so every rescale of O and of the row sum is an exact power of two.
 #pragma once
 
 #include "sm100.cuh"
@@ -45,18 +41,17 @@ constexpr int kPfAtom = 128 * 128;  // 128 rows x 64 bf16 columns (one swizzle a
 constexpr int kPfQ = 3 * kPfAtom;   // q^C (two atoms) + q^R (one)
 constexpr int kPfK = 3 * kPfAtom;   // k^C (two atoms) + k^R (one)
 constexpr int kPfV = 2 * kPfAtom;   // v^C (two atoms)
-constexpr int kPfKStages = 3;  // the key ring; an item's Q passes through it first
-constexpr int kPfVStages = 2;
-constexpr int kPfOffK = 0;
+constexpr int kPfKStages = 2, kPfVStages = 2;
+static_assert(kPfKStages == 2 && kPfVStages == 2, "the producers index two-deep rings");
+constexpr int kPfOffK = kPfQ;
 constexpr int kPfOffV = kPfOffK + kPfKStages * kPfK;
 constexpr int kPfOffBar = kPfOffV + kPfVStages * kPfV;
 enum : int {
-  PF_KFULL = 0, PF_KEMPTY = 3, PF_VFULL = 6, PF_VEMPTY = 8, PF_SFULL = 10, PF_PREADY = 12, PF_PVDONE = 14,
-  PF_OFREE = 16, PF_QDONE = 17, PF_DRAIN = 18, PF_NBARS = 19
+  PF_QFULL = 0, PF_QEMPTY = 1, PF_KFULL = 2, PF_KEMPTY = 4, PF_VFULL = 6, PF_VEMPTY = 8,
+  PF_SFULL = 10, PF_PREADY = 13, PF_PVDONE = 16, PF_OFREE = 19, PF_DRAIN = 20, PF_NBARS = 21
 };
 constexpr size_t kPfSmem = (size_t)kPfOffBar + PF_NBARS * 8 + 16;
-// tensor memory: score buffers at columns 0 and 128, O at 256, Q (bf16, 96 columns) at 384
-constexpr uint32_t kPfOCol = 256, kPfQCol = 384;
+constexpr uint32_t kPfOCol = 384;  // O; the score buffers sit at columns 0, 128 and 256
 
 struct PrefillParams {
   __nv_bfloat16* out;        // [B, S, H, 128]
@@ -164,7 +159,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   if (threadIdx.x == 0) {
     *abort_flag = 0u;
     for (int i = 0; i < PF_NBARS; ++i) {
-      const bool per_thread = (i >= PF_PREADY && i < PF_PREADY + 2) || i == PF_OFREE;
+      const bool per_thread = (i >= PF_PREADY && i < PF_PREADY + 3) || i == PF_OFREE;
       mbar_init(&bar[i], per_thread ? 128u : 1u);
     }
     fence_mbar_init_cluster();
@@ -191,7 +186,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       // loads Q and the key tiles, warp 2 the value tiles, each on its own ring
       // so that neither waits for the other's slots
       const bool keys = warp == 0;
-      uint32_t c = 0;
+      uint32_t c = 0, it = 0, q_issued = 0;
       bool ok = true;
       PfIter iter;
       PfItem ii;
@@ -200,24 +195,19 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           if (keys) atomicOr(p.status, kDevErrBadSeqlen);
           continue;
         }
-        if (keys) {  // the item's Q takes the next key stage
-          const uint32_t st = c % kPfKStages;
-          if (c >= (uint32_t)kPfKStages &&
-              !mbar_wait(&bar[PF_KEMPTY + st], ((c / kPfKStages) - 1) & 1u, wc))
-            break;
+        if (keys) {
+          if (it > 0 && !mbar_wait(&bar[PF_QEMPTY], (it - 1) & 1u, wc)) break;
           const int qrow = ii.b * p.S + ii.s0;
-          uint8_t* qb = smem + kPfOffK + st * kPfK;
-          mbar_arrive_expect_tx(&bar[PF_KFULL + st], (uint32_t)kPfQ);
-          tma_load_4d(qb, &tm_qn, &bar[PF_KFULL + st], 0, qrow, 0, ii.h);
-          tma_load_3d(qb + 2 * kPfAtom, &tm_qr, &bar[PF_KFULL + st], 0, qrow, ii.h);
-          ++c;
+          mbar_arrive_expect_tx(&bar[PF_QFULL], (uint32_t)kPfQ);
+          tma_load_4d(smem, &tm_qn, &bar[PF_QFULL], 0, qrow, 0, ii.h);
+          tma_load_3d(smem + 2 * kPfAtom, &tm_qr, &bar[PF_QFULL], 0, qrow, ii.h);
+          q_issued = it + 1;
         }
         const int krow0 = ii.b * p.Lmax;
-        const uint32_t ns = keys ? kPfKStages : kPfVStages;
         for (int t = 0; t < ii.nt; ++t, ++c) {
           const int krow = krow0 + t * 128;
-          const uint32_t st = c % ns;
-          if (c >= ns && !mbar_wait(&bar[(keys ? PF_KEMPTY : PF_VEMPTY) + st], ((c / ns) - 1) & 1u, wc)) {
+          const uint32_t st = c % 2;  // both rings are two deep
+          if (c >= 2 && !mbar_wait(&bar[(keys ? PF_KEMPTY : PF_VEMPTY) + st], ((c / 2) - 1) & 1u, wc)) {
             ok = false;
             break;
           }
@@ -232,11 +222,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             tma_load_4d(smem + kPfOffV + st * kPfV, &tm_vc, &bar[PF_VFULL + st], 0, krow, 0, ii.h);
           }
         }
+        ++it;
       }
       // every copy issued lands before the CTA winds down
       const int full = keys ? PF_KFULL : PF_VFULL;
-      const uint32_t ns = keys ? kPfKStages : kPfVStages;
-      for (uint32_t j = c > ns ? c - ns : 0; j < c; ++j) mbar_wait_drain(&bar[full + j % ns], (j / ns) & 1u, wc);
+      for (uint32_t j = c > 2u ? c - 2 : 0; j < c; ++j) mbar_wait_drain(&bar[full + j % 2], (j / 2) & 1u, wc);
+      if (q_issued > 0) mbar_wait_drain(&bar[PF_QFULL], (q_issued - 1) & 1u, wc);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -245,37 +236,20 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       constexpr uint32_t idv = idesc_bf16_f32(128, 128, 0, 1);  // O += P V, V MN-major
       uint32_t kc = 0, vc = 0, g = 0, it = 0;
       bool ok = true;
-      // The item's Q (the next key stage) into tensor memory, once the
-      // previous item's QK^T, which read the old Q there, have completed.
-      auto take_q = [&]() -> bool {
-        const uint32_t st = kc % kPfKStages;
-        if (!mbar_wait(&bar[PF_KFULL + st], (kc / kPfKStages) & 1u, wc)) return false;
-        if (it > 0 && !mbar_wait(&bar[PF_QDONE], (it - 1) & 1u, wc)) return false;
-        tc_fence_after();
-        const uint32_t qa = smem_u32(smem + kPfOffK + st * kPfK);
-#pragma unroll
-        for (int kk = 0; kk < 12; ++kk)  // 128 rows x 16 columns (8 tensor-memory columns) each
-          tmem_cp_128x256b(tmem + kPfQCol + (uint32_t)kk * 8,
-                           smem_desc(qa + (uint32_t)((kk >> 2) * kPfAtom + (kk & 3) * 32), 16, 1024, 2));
-        mma_commit(&bar[PF_KEMPTY + st]);  // the stage is free once the copies are done
-        ++kc;
-        return true;
-      };
-      // QK^T of the tile with running index gg into score buffer gg % 2, whose
-      // previous P (tile gg - 2) must have been consumed by its P.V.  Q comes
-      // from tensor memory (ordered after take_q's copies), K from shared memory.
+      // QK^T of the tile with running index gg into score buffer gg % 3, whose
+      // previous P (tile gg - 3) must have been consumed by its P.V.
       auto qk = [&](uint32_t gg) -> bool {
-        const uint32_t sb = gg & 1u;
-        if (gg >= 2 && !mbar_wait(&bar[PF_PVDONE + sb], ((gg >> 1) - 1) & 1u, wc)) return false;
+        const uint32_t sb = gg % 3;
+        if (gg >= 3 && !mbar_wait(&bar[PF_PVDONE + sb], ((gg / 3) - 1) & 1u, wc)) return false;
         const uint32_t st = kc % kPfKStages;
         if (!mbar_wait(&bar[PF_KFULL + st], (kc / kPfKStages) & 1u, wc)) return false;
         PF_TRACE(p, PT_KFULL, gg);
         tc_fence_after();
-        const uint32_t ka = smem_u32(smem + kPfOffK + st * kPfK);
+        const uint32_t qa = smem_u32(smem), ka = smem_u32(smem + kPfOffK + st * kPfK);
 #pragma unroll
         for (int kk = 0; kk < 12; ++kk) {  // 192 = 3 atoms x 4 K-steps of 16
           const uint32_t off = (uint32_t)((kk >> 2) * kPfAtom + (kk & 3) * 32);
-          mma_ts(tmem + sb * 128, tmem + kPfQCol + (uint32_t)kk * 8, smem_desc(ka + off, 16, 1024, 2), idq,
+          mma_ss(tmem + sb * 128, smem_desc(qa + off, 16, 1024, 2), smem_desc(ka + off, 16, 1024, 2), idq,
                  kk > 0 ? 1u : 0u);
         }
         mma_commit(&bar[PF_KEMPTY + st]);
@@ -288,15 +262,13 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       PfItem ii;
       while (ok && iter.next(p, ii)) {
         if (!ii.ok) continue;
-        if (!take_q() || !qk(g)) break;
+        // QK^T runs two tiles ahead of P.V: while the softmax works on tile t,
+        // the scores of tiles t + 1 and t + 2 are computed or ready
+        if (!mbar_wait(&bar[PF_QFULL], it & 1u, wc) || !qk(g) || (ii.nt > 1 && !qk(g + 1))) break;
+        if (ii.nt <= 2) mma_commit(&bar[PF_QEMPTY]);  // Q is free once these QK^T are done
         for (int t = 0; t < ii.nt; ++t) {
-          if (t + 1 < ii.nt && !qk(g + 1)) {
-            ok = false;
-            break;
-          }
-          if (t + 1 == ii.nt) mma_commit(&bar[PF_QDONE]);  // Q may be replaced once these QK^T are done
-          const uint32_t sb = g & 1u, st = vc % kPfVStages;
-          if (!mbar_wait(&bar[PF_PREADY + sb], (g >> 1) & 1u, wc) ||
+          const uint32_t sb = g % 3, st = vc % kPfVStages;
+          if (!mbar_wait(&bar[PF_PREADY + sb], (g / 3) & 1u, wc) ||
               (t == 0 && it > 0 && !mbar_wait(&bar[PF_OFREE], (it - 1) & 1u, wc))) {
             ok = false;
             break;
@@ -332,6 +304,13 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           PF_TRACE(p, PT_PV, g);
           ++vc;
           ++g;
+          if (t + 2 < ii.nt) {  // tile t + 2 (running index g + 1) into the buffer P.V of t - 1 freed
+            if (!qk(g + 1)) {
+              ok = false;
+              break;
+            }
+            if (t + 3 == ii.nt) mma_commit(&bar[PF_QEMPTY]);
+          }
         }
         ++it;
       }
@@ -352,8 +331,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       const int pr = min(ii.p0 + r, ii.p_last);  // rows past the block's last query repeat it
       float m_ref = -INFINITY, l = 0.f;
       for (int t = 0; t < ii.nt; ++t) {
-        const uint32_t sb = g & 1u;
-        if (!pf_warp_wait(&bar[PF_SFULL + sb], (g >> 1) & 1u, wc)) {
+        const uint32_t sb = g % 3;
+        if (!pf_warp_wait(&bar[PF_SFULL + sb], (g / 3) & 1u, wc)) {
           ok = false;
           break;
         }
@@ -392,7 +371,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         const bool need = t > 0 && ex != 0;
         if (__any_sync(0xffffffffu, need)) {
           // O holds this item's earlier tiles once the previous P.V has completed
-          if (!pf_warp_wait(&bar[PF_PVDONE + ((g - 1) & 1u)], ((g - 1) >> 1) & 1u, wc)) {
+          if (!pf_warp_wait(&bar[PF_PVDONE + (g - 1) % 3], ((g - 1) / 3) & 1u, wc)) {
             ok = false;
             break;
           }
@@ -445,7 +424,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       }
       if (!ok) break;
       // epilogue: out = O / l once the item's last P.V has completed
-      if (!pf_warp_wait(&bar[PF_PVDONE + ((g - 1) & 1u)], ((g - 1) >> 1) & 1u, wc)) break;
+      if (!pf_warp_wait(&bar[PF_PVDONE + (g - 1) % 3], ((g - 1) / 3) & 1u, wc)) break;
       tc_fence_after();
       const float inv = 1.f / l;
       const bool valid = r < ii.nrow;
