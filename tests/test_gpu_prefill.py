@@ -142,3 +142,25 @@ def test_out_of_range_length_is_reported_and_skipped():
     ref = oracle.prefill_attention(bits(t["q_nope"])[:1], bits(t["q_rot"])[:1], bits(t["k_c"])[:1],
                                    bits(t["k_r"])[:1], bits(t["v_c"])[:1], L[:1], softmax_scale=SCALE)
     assert_close(f64(out[:1]), ref, what="the valid sequence")
+
+
+def test_prefill_bench_workload_heads_match_oracle():
+    """The benchmark's prefill (4 prompts of 4096 tokens, 128 heads, the same
+    seeded inputs): every query row of three (sequence, head) pairs, against the
+    oracle's own expansion, RoPE and causal attention for those heads."""
+    B, S, H = 4, 4096, 128
+    x = make_inputs(B, S, H, [S] * B, seed=68005)
+    d = to_dev(x)
+    mb.rope_cache(d["k_r"], d["seqlens"])
+    step = mb.PrefillStep(B, S, H, S)
+    out = step(d["q_nope"], d["q_rope"], d["c_kv"], d["k_r"], d["seqlens"], d["W_UK"], d["W_UV"])
+    assert mb.read_status() == mb.MLA_OK
+    qn, qr, ck, kr = (bits(x[k]) for k in ("q_nope", "q_rope", "c_kv", "k_r"))
+    wk, wv = bits(x["W_UK"]), bits(x["W_UV"])
+    for b, h in [(0, 0), (3, 127), (1, 77)]:
+        kc = oracle.expand_kv(ck[b:b + 1], wk[h:h + 1])                     # [1, S, 1, 128]
+        vc = oracle.expand_kv(ck[b:b + 1], wv[h:h + 1])
+        q_rot = oracle.rope(qr[b, :, h], np.arange(S)).reshape(1, S, 1, 64)  # query s at position s
+        k_rot = oracle.rope(kr[b], np.arange(S)).reshape(1, S, 64)
+        ref = oracle.prefill_attention(qn[b:b + 1, :, h:h + 1], q_rot, kc, k_rot, vc, [S], softmax_scale=SCALE)
+        assert_close(f64(out[b, :, h]), ref[0, :, 0], what=f"prefill 4x4096 sequence {b} head {h}")
