@@ -250,7 +250,7 @@ def _time_append(args, x, d, dev, stream, flush_l2, theta, mb):
     us = statistics.mean(e[0].elapsed_time(e[1]) for e in ev) * 1000
     nbytes = (512 + 64) * APPEND_D * 2 + B * S * APPEND_D * 2 + B * S * (512 + 64) * 2
     return {"workload": f"B={B} S={S} new tokens, d={APPEND_D}", "us": round(us, 3), "bytes": nbytes,
-            "launches": 2}
+            "launches": 1, "form": "one cooperative launch (GEMM, grid barrier, finalize)"}
 
 
 class Packed:

@@ -259,9 +259,13 @@ size_t mla_cache_append_workspace_size(int B, int S, int d);
  *   theta  host [32] RoPE frequencies (mla_rope_yarn_frequencies), or NULL
  *          for theta_j = 10000^(-2j/64)
  *   workspace >= mla_cache_append_workspace_size(B, S, d) bytes, 256-byte
- *          aligned; its first word is a status word (mla_read_status): a
- *          position outside [0, Lmax) sets MLA_ERR_BAD_SEQLEN and skips the
- *          token.
+ *          aligned, zero-filled before its first use; its first word is a
+ *          status word (mla_read_status): a position outside [0, Lmax) sets
+ *          MLA_ERR_BAD_SEQLEN and skips the token.  Words 1 and 2 hold a
+ *          grid-wide barrier that each call leaves as it found it; after a
+ *          call that reported MLA_ERR_TIMEOUT, zero-fill the workspace again.
+ * One cooperative launch when all of its CTAs fit on the device at once
+ * (the finalize follows a grid-wide barrier), else two launches.
  * The weights are read before the kernel waits for the one launched before
  * it on the stream, so they must not be written by that kernel.
  */

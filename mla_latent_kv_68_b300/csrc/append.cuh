@@ -11,10 +11,12 @@
 // the 64 rows of W^KR), the tokens take N, and d is cut into slices of
 // kAppKc columns, one CTA per (weight tile, slice, token tile), so that about
 // a hundred SMs stream the 8 MB of weights at once.  Each CTA leaves its fp32
-// partial product in a workspace; the finalize kernel sums the slices in a
-// fixed order (the result does not depend on timing), rotates the k^R part
-// at the token's position (fp64 angle reduction, as rope.cuh) and writes
-// both parts, rounded to bf16, into the cache rows.
+// partial product in a workspace; the finalize sums the slices in a fixed
+// order (the result does not depend on timing), rotates the k^R part at the
+// token's position (fp64 angle reduction, as rope.cuh) and writes both parts,
+// rounded to bf16, into the cache rows.  When all CTAs fit on the GPU at once
+// the finalize runs in the same (cooperative) launch after a grid-wide
+// barrier; otherwise a second kernel does it.
 #pragma once
 
 #include "rope.cuh"
@@ -26,13 +28,65 @@ constexpr int kAppThreads = 128;
 constexpr int kAppKc = 256;    // d columns per CTA: four 64-column atoms
 constexpr int kAppCols = 576;  // d_c + d_h^R
 
+struct AppendFinalizeParams {
+  const float* part;       // [ks][BS][576]
+  const int32_t* seqlens;  // [B]: the new tokens sit at seqlens[b] - S .. seqlens[b] - 1
+  __nv_bfloat16* c_kv;     // [B, Lmax, 512]
+  __nv_bfloat16* k_r;      // [B, Lmax, 64]
+  uint32_t* status;
+  int BS, S, ks, Lmax;
+};
+
 struct AppendParams {
   float* part;        // [ks][BS][576] fp32 partial products
   int BS, n_tile, ks;
   uint32_t tmem_cols;
   uint32_t* status;
   uint64_t timeout_ns;
+  uint32_t* barrier;  // fused form: [0] arrivals, [1] generation (zero-filled workspace words)
+  int fused;          // 1: finalize in this launch after a grid-wide barrier (cooperative launch)
+  AppendFinalizeParams fin;
 };
+
+// Output pair t (0..287) of token n: the slices summed in order; pairs 0..255
+// are c^KV, pairs 256..287 the k^R pairs, turned by pos * theta_j.
+__device__ __forceinline__ void append_finalize_pair(const AppendFinalizeParams& p, const RopeTheta& th, int n,
+                                                     int t) {
+  const int b = n / p.S, s = n - b * p.S;
+  const int64_t pos = (int64_t)p.seqlens[b] - p.S + s;
+  if (pos < 0 || pos >= p.Lmax) {
+    if (t == 0) atomicOr(p.status, kDevErrBadSeqlen);
+    return;
+  }
+  const float2* src = reinterpret_cast<const float2*>(p.part + (size_t)n * kAppCols) + t;
+  const size_t kstep = (size_t)p.BS * kAppCols / 2;  // float2 elements between slices
+  // the slices (28 at d = 7168) are requested together, then summed in order;
+  // read through L2 (.cg), since in the fused form they were written by this launch
+  float x = 0.f, y = 0.f;
+  for (int k0 = 0; k0 < p.ks; k0 += 32) {
+    float2 v[32];
+#pragma unroll
+    for (int u = 0; u < 32; ++u) v[u] = k0 + u < p.ks ? __ldcg(src + (size_t)(k0 + u) * kstep) : make_float2(0.f, 0.f);
+#pragma unroll
+    for (int u = 0; u < 32; ++u) {
+      x += v[u].x;
+      y += v[u].y;
+    }
+  }
+  if (t < 256) {
+    reinterpret_cast<__nv_bfloat162*>(p.c_kv + ((size_t)b * p.Lmax + pos) * 512)[t] = __floats2bfloat162_rn(x, y);
+  } else {
+    const int j = t - 256;
+    const double two_pi = 6.283185307179586476925286766559;
+    const double inv_two_pi = 0.15915494309189533576888376337251;
+    const double a = (double)pos * th.theta[j];
+    const double rr = fma(-rint(a * inv_two_pi), two_pi, a);
+    float sn, cs;
+    sincosf((float)rr, &sn, &cs);
+    reinterpret_cast<__nv_bfloat162*>(p.k_r + ((size_t)b * p.Lmax + pos) * 64)[j] =
+        __floats2bfloat162_rn(x * cs - y * sn, x * sn + y * cs);
+  }
+}
 
 __host__ __device__ constexpr size_t app_smem_bytes(int n_tile) {
   return (size_t)4 * 16384 + (size_t)4 * n_tile * 128 + 64;
@@ -40,7 +94,7 @@ __host__ __device__ constexpr size_t app_smem_bytes(int n_tile) {
 
 __global__ void __launch_bounds__(kAppThreads, 1)
     append_gemm_kernel(const __grid_constant__ CUtensorMap tm_wd, const __grid_constant__ CUtensorMap tm_wr,
-                       const __grid_constant__ CUtensorMap tm_h, const AppendParams p) {
+                       const __grid_constant__ CUtensorMap tm_h, const AppendParams p, const RopeTheta th) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const int mt = blockIdx.x;       // 0..3: W^DKV rows 128 mt ..; 4: W^KR
   const int split = blockIdx.y;    // d columns split * kAppKc ..
@@ -115,6 +169,7 @@ __global__ void __launch_bounds__(kAppThreads, 1)
         if (live && c0 + c < nvalid) dst[(size_t)(c0 + c) * kAppCols] = __uint_as_float(r[c]);
     }
   }
+  __threadfence();  // the partial product is visible device-wide before this CTA arrives below
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -122,56 +177,50 @@ __global__ void __launch_bounds__(kAppThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, p.tmem_cols);
   }
+  if (!p.fused) return;
+  // Fused form (a cooperative launch: every CTA is resident): a grid-wide
+  // barrier on two workspace words -- arrivals, reset by the last CTA to
+  // arrive, which then bumps the generation the others wait on (bounded) --
+  // and then every CTA finalizes its share of the output pairs.
+  volatile uint32_t* go = tmem_slot;  // reused: 1 = the barrier completed
+  if (threadIdx.x == 0) {
+    const uint32_t total = gridDim.x * gridDim.y * gridDim.z;
+    volatile uint32_t* gen = p.barrier + 1;
+    const uint32_t g0 = *gen;
+    uint32_t passed = 1u;
+    if (atomicAdd(p.barrier, 1u) == total - 1u) {
+      atomicExch(p.barrier, 0u);
+      __threadfence();
+      atomicAdd(p.barrier + 1, 1u);
+    } else {
+      const uint64_t t0 = global_timer_ns();
+      while (*gen == g0) {
+        if (global_timer_ns() - t0 > p.timeout_ns) {
+          atomicOr(p.status, kDevErrTimeout);
+          passed = 0u;
+          break;
+        }
+        __nanosleep(100);
+      }
+    }
+    __threadfence();
+    *go = passed;
+  }
+  __syncthreads();
+  if (!*go) return;
+  const int total = (int)(gridDim.x * gridDim.y * gridDim.z);
+  const int cta = (int)(blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z));
+  const int pairs = p.BS * (kAppCols / 2);
+  for (int i = cta * kAppThreads + (int)threadIdx.x; i < pairs; i += total * kAppThreads)
+    append_finalize_pair(p.fin, th, i / (kAppCols / 2), i % (kAppCols / 2));
 }
-
-struct AppendFinalizeParams {
-  const float* part;       // [ks][BS][576]
-  const int32_t* seqlens;  // [B]: the new tokens sit at seqlens[b] - S .. seqlens[b] - 1
-  __nv_bfloat16* c_kv;     // [B, Lmax, 512]
-  __nv_bfloat16* k_r;      // [B, Lmax, 64]
-  uint32_t* status;
-  int BS, S, ks, Lmax;
-};
 
 // Block = one token, thread = one pair of output columns (288 per token).
 __global__ void __launch_bounds__(kAppCols / 2)
     append_finalize_kernel(const AppendFinalizeParams p, const RopeTheta th) {
   pdl_trigger();
   pdl_wait();  // the partial products come from the GEMM kernel
-  const int n = blockIdx.x, t = threadIdx.x;
-  const int b = n / p.S, s = n - b * p.S;
-  const int64_t pos = (int64_t)p.seqlens[b] - p.S + s;
-  if (pos < 0 || pos >= p.Lmax) {
-    if (t == 0) atomicOr(p.status, kDevErrBadSeqlen);
-    return;
-  }
-  const float2* src = reinterpret_cast<const float2*>(p.part + (size_t)n * kAppCols) + t;
-  const size_t kstep = (size_t)p.BS * kAppCols / 2;  // float2 elements between slices
-  // the slices (28 at d = 7168) are requested together, then summed in order
-  float x = 0.f, y = 0.f;
-  for (int k0 = 0; k0 < p.ks; k0 += 32) {
-    float2 v[32];
-#pragma unroll
-    for (int u = 0; u < 32; ++u) v[u] = k0 + u < p.ks ? src[(size_t)(k0 + u) * kstep] : make_float2(0.f, 0.f);
-#pragma unroll
-    for (int u = 0; u < 32; ++u) {
-      x += v[u].x;
-      y += v[u].y;
-    }
-  }
-  if (t < 256) {
-    reinterpret_cast<__nv_bfloat162*>(p.c_kv + ((size_t)b * p.Lmax + pos) * 512)[t] = __floats2bfloat162_rn(x, y);
-  } else {  // pair j of k^R, turned by pos * theta_j
-    const int j = t - 256;
-    const double two_pi = 6.283185307179586476925286766559;
-    const double inv_two_pi = 0.15915494309189533576888376337251;
-    const double a = (double)pos * th.theta[j];
-    const double rr = fma(-rint(a * inv_two_pi), two_pi, a);
-    float sn, cs;
-    sincosf((float)rr, &sn, &cs);
-    reinterpret_cast<__nv_bfloat162*>(p.k_r + ((size_t)b * p.Lmax + pos) * 64)[j] =
-        __floats2bfloat162_rn(x * cs - y * sn, x * sn + y * cs);
-  }
+  append_finalize_pair(p, th, blockIdx.x, threadIdx.x);
 }
 
 }  // namespace mla

@@ -627,12 +627,8 @@ mla_status mla_cache_append(const mla_bf16* h, const mla_bf16* W_DKV, const mla_
   p.tmem_cols = pow2_at_least((uint32_t)n_tile);
   p.status = reinterpret_cast<uint32_t*>(ws);
   p.timeout_ns = kTimeoutNs;
-  cudaStream_t st = (cudaStream_t)stream;
-  const dim3 grid(5, (unsigned)ks, (unsigned)((BS + n_tile - 1) / n_tile));
-  const mla_status s1 = launch_ex(mla::append_gemm_kernel, grid, dim3(mla::kAppThreads),
-                                  mla::app_smem_bytes(n_tile), st, true, 1, twd, twr, th_map, p);
-  if (s1 != MLA_OK) return s1;
-  mla::AppendFinalizeParams f;
+  p.barrier = reinterpret_cast<uint32_t*>(ws) + 1;  // words 1 (arrivals) and 2 (generation)
+  mla::AppendFinalizeParams& f = p.fin;
   f.part = p.part;
   f.seqlens = seqlens;
   f.c_kv = reinterpret_cast<__nv_bfloat16*>(c_kv);
@@ -642,8 +638,38 @@ mla_status mla_cache_append(const mla_bf16* h, const mla_bf16* W_DKV, const mla_
   f.S = S;
   f.ks = ks;
   f.Lmax = Lmax;
+  cudaStream_t st = (cudaStream_t)stream;
+  const dim3 grid(5, (unsigned)ks, (unsigned)((BS + n_tile - 1) / n_tile));
+  const size_t smem = mla::app_smem_bytes(n_tile);
+  // One cooperative launch (the finalize after a grid-wide barrier) when every
+  // CTA can be resident at once; otherwise the GEMM and the finalize kernel.
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, mla::append_gemm_kernel, mla::kAppThreads, smem) !=
+      cudaSuccess)
+    return MLA_ERR_CUDA;
+  const long long ctas = 5LL * ks * grid.z;
+  if (ctas <= (long long)per_sm * dev->num_sms) {
+    p.fused = 1;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(mla::kAppThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, mla::append_gemm_kernel, twd, twr, th_map, p, th) != cudaSuccess)
+      return MLA_ERR_CUDA;
+    return launch_status();
+  }
+  p.fused = 0;
+  const mla_status s1 = launch_ex(mla::append_gemm_kernel, grid, dim3(mla::kAppThreads), smem, st, true, 1, twd,
+                                  twr, th_map, p, th);
+  if (s1 != MLA_OK) return s1;
   return launch_ex(mla::append_finalize_kernel, dim3((unsigned)BS), dim3(mla::kAppCols / 2), 0, st, true, 1,
-                   f, th);
+                   p.fin, th);
 }
 
 mla_status mla_debug_decode_stall(uint64_t wait_limit_ns) {
