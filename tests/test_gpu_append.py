@@ -78,6 +78,9 @@ def _check(c, k, h, wd, wr, seqlens, theta=None, skip=()):
     (4, 1, 7168, [1, 100, 131072, 65536], 131072),
     (33, 1, 1024, list(range(1, 34)), 40),
     (150, 2, 512, [2 + (i * 37) % 900 for i in range(150)], 1000),
+    # 600 tokens at d = 7168: 5 x 28 x 3 CTAs, more than can be resident at
+    # once, so the GEMM and the finalize run as two launches
+    (300, 2, 7168, [2 + (i * 53) % 500 for i in range(300)], 600),
 ])
 def test_cache_append_matches_oracle(B, S, d, seqlens, Lmax):
     h, wd, wr = _case(B, S, d, seed=B * 7 + S * 3 + d)
