@@ -205,8 +205,16 @@ struct TileInfo {
 
 // The split plan as one CTA needs it (splitkv.cuh): the total tile count and
 // the state of the walk at the sequence holding the group's first tile.
+// The split plan lays all sequences end to end in units of work: one unit
+// per 128-token tile, after kSeqUnits units that stand for the cost of
+// starting a sequence (a cluster that switches to another sequence passes the
+// query rows through its ring again and writes one more partial result), and
+// cuts them into G equal runs.  A run that falls on those units alone has no
+// tile there.
+constexpr int kSeqUnits = 1;
+
 struct PlanState {
-  int64_t T;       // tiles of all sequences
+  int64_t T;       // units of all sequences
   int b0, x0, sb0;  // that sequence, its first flat tile, its first segment slot
   int ok;          // every sequence length was valid
 };
@@ -234,7 +242,7 @@ __device__ void plan_scan(const DecodeParams& p, int g, bool write_global, PlanS
     for (int u = 0; u < 8; ++u) {
       if (base + u * 32 + lane >= p.B) continue;
       if (L[u] < p.S || L[u] > p.Lmax) bad = true;
-      else t += tiles_of(L[u]);
+      else t += kSeqUnits + tiles_of(L[u]);
     }
     T += __reduce_add_sync(0xffffffffu, (unsigned)t);
   }
@@ -246,14 +254,16 @@ __device__ void plan_scan(const DecodeParams& p, int g, bool write_global, PlanS
   for (int base = 0; base < p.B && !bad && (write_global || !found); base += 32) {  // pass 2
     const int b = base + lane;
     const int t = b < p.B ? tiles_of(p.seqlens[b]) : 0;
-    int it = t;  // inclusive scans over the warp
+    const int un = b < p.B ? kSeqUnits + t : 0;  // the sequence's units
+    int it = un;  // inclusive scans over the warp
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int y = __shfl_up_sync(0xffffffffu, it, o);
       if (lane >= o) it += y;
     }
-    const int64_t x = run_x + it - t;  // first flat tile of sequence b
-    const int ns = nseg_of(x, x + t, T, p.G);
+    const int64_t x = run_x + it - un;  // first unit of sequence b
+    const int64_t xr = x + kSeqUnits;    // the unit of its first tile
+    const int ns = nseg_of(xr, xr + t, T, p.G);
     int is = ns;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -262,11 +272,11 @@ __device__ void plan_scan(const DecodeParams& p, int g, bool write_global, PlanS
     }
     const int sb = run_sb + is - ns;  // its first segment slot
     if (write_global && b < p.B) {
-      p.prefix[b] = (int32_t)x;
-      p.gfirst[b] = t > 0 ? group_of(x, T, p.G) : 0;
+      p.prefix[b] = (int32_t)xr;
+      p.gfirst[b] = t > 0 ? group_of(xr, T, p.G) : 0;
       p.segbase[b] = sb;
     }
-    const unsigned hit = __ballot_sync(0xffffffffu, t > 0 && x <= beg && beg < x + t);
+    const unsigned hit = __ballot_sync(0xffffffffu, t > 0 && x <= beg && beg < x + un);
     if (!found && hit) {
       const int src = __ffs(hit) - 1;
       b0 = __shfl_sync(0xffffffffu, b, src);
@@ -295,8 +305,8 @@ __device__ void plan_scan(const DecodeParams& p, int g, bool write_global, PlanS
 // Tiles of group g in order, as a cursor that follows the sequences from the
 // plan state on (prefix and segment slot carried along, lengths re-read).
 struct TileCursor {
-  int64_t beg, end, T;  // the group's flat tiles [beg, end) of T
-  int64_t x0;           // first flat tile of sequence b
+  int64_t beg, end, T;  // the group's units [beg, end) of T
+  int64_t x0;           // first unit of sequence b
   int g, b, sb, t, tb, te, i, k, slot, L;
 };
 
@@ -304,16 +314,16 @@ struct TileCursor {
 __device__ __forceinline__ bool cursor_seq(const DecodeParams& p, TileCursor& c) {
   while (c.b < p.B && c.x0 < c.end) {
     const int L = p.seqlens[c.b];
-    const int64_t x1 = c.x0 + tiles_of(L);
-    if (x1 > c.beg) {
-      c.tb = (int)(max(c.beg, c.x0) - c.x0);
-      c.te = (int)(min(c.end, x1) - c.x0);
+    const int64_t xr = c.x0 + kSeqUnits, x1 = xr + tiles_of(L);
+    if (x1 > c.beg && min(c.end, x1) > max(c.beg, xr)) {
+      c.tb = (int)(max(c.beg, xr) - xr);
+      c.te = (int)(min(c.end, x1) - xr);
       c.t = c.tb;
-      c.slot = c.sb + (c.g - group_of(c.x0, c.T, p.G));
+      c.slot = c.sb + (c.g - group_of(xr, c.T, p.G));
       c.L = L;
       return true;
     }
-    c.sb += nseg_of(c.x0, x1, c.T, p.G);
+    c.sb += nseg_of(xr, x1, c.T, p.G);
     c.x0 = x1;
     ++c.b;
   }
@@ -339,8 +349,8 @@ __device__ __forceinline__ bool cursor_next(const DecodeParams& p, TileCursor& c
   ++c.i;
   if (++c.t < c.te) return true;
   ++c.k;
-  const int64_t x1 = c.x0 + tiles_of(c.L);
-  c.sb += nseg_of(c.x0, x1, c.T, p.G);
+  const int64_t xr = c.x0 + kSeqUnits, x1 = xr + tiles_of(c.L);
+  c.sb += nseg_of(xr, x1, c.T, p.G);
   c.x0 = x1;
   ++c.b;
   return cursor_seq(p, c);

@@ -12,11 +12,12 @@
 //     o_lat = sum_k w_k U_k / sum_k w_k,   w_k = 2^(m_k - M) l_k,   M = max_k m_k.
 //
 // Tiles are kTileRows = 128 cache rows (the N of the decode's QK^T MMAs).
-// Plan: the cache tiles of all sequences are laid end to end (sequence-major)
-// and cut into G equal runs, one per group of clusters.  Group g owns flat
-// tiles [floor(g T / G), floor((g+1) T / G)).  A sequence b contributes one
-// segment to every group its tiles touch; its segments get consecutive slot
-// numbers starting at segbase[b].  The decode kernel works the plan out
+// Plan: the cache tiles of all sequences are laid end to end (sequence-major),
+// each sequence's tiles after one unit that stands for the cost of starting
+// it, and the T units are cut into G equal runs, one per group of clusters.
+// Group g owns units [floor(g T / G), floor((g+1) T / G)).  A sequence b
+// contributes one segment to every group its tiles touch; its segments get
+// consecutive slot numbers starting at segbase[b].  The decode kernel works the plan out
 // itself from the sequence lengths (decode.cuh, plan_scan) and leaves the
 // arrays below (prefix, gfirst, segbase, plan_ok) for the combine.
 #pragma once
@@ -35,7 +36,7 @@ __device__ __forceinline__ int group_of(int64_t x, int64_t T, int G) {
 }
 
 struct CombineParams {
-  const int32_t* prefix;   // plan: prefix[B] = total tiles T
+  const int32_t* prefix;   // plan: prefix[b] = the unit of b's first tile, prefix[B] = total units T
   const int32_t* gfirst;
   const int32_t* segbase;
   const float2* ml;     // [slots * n_rb, 128] (m_k, l_k)
