@@ -391,12 +391,16 @@ __device__ __forceinline__ void for_each_tile_warm(const DecodeParams& p, int g,
   }
 }
 
-// Score-CTA c-ring positions for tile i of segment k.  Every segment first
-// sends its 512 q~ columns through the c ring (two stages), every tile its
-// cache rows (the same); c stage h holds blocks 4h .. 4h + 3.  The k^R ring
+// Score-CTA c-ring positions for tile i of segment k.  Every segment sends
+// its 512 q~ columns through the c ring (two stages), every tile its cache
+// rows (the same); stage h holds blocks 4h .. 4h + 3.  A segment's first
+// tile interleaves them (q~ half 0, c half 0, q~ half 1, c half 1), so that
+// its first QK^T half waits for two copies rather than three.  The k^R ring
 // carries cache rows only (tile i at position i); q^R has its own buffer.
-__device__ __forceinline__ int cpos_q(int i, int k, int h) { return kCPerTile * (i + k) + h; }
-__device__ __forceinline__ int cpos_kv(int i, int k, int h) { return kCPerTile * (i + k + 1) + h; }
+__device__ __forceinline__ int cpos_q(int i, int k, int h) { return kCPerTile * (i + k) + 2 * h; }
+__device__ __forceinline__ int cpos_kv(int i, int k, int h, bool first) {
+  return first ? kCPerTile * (i + k) + 2 * h + 1 : kCPerTile * (i + k + 1) + h;
+}
 constexpr int kBarC = 0, kBarR = kCStages;  // FULL / EMPTY sub-ranges of the two rings
 
 // All 32 lanes wait; the outcome is made warp-uniform so that warp-collective
@@ -555,13 +559,11 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       for_each_tile(p, g, *plan, [&](const TileInfo& ti) {
         const int row0 = ti.b * p.Lmax + ti.t * kTok;
         if (rank == 0) {
-          if (ti.first) {  // the segment's query rows: blocks 0..7 through the c ring, q^R to its buffer
-            const int qrow0 = ti.b * SH + rb * 128;
-            for (int h = 0; h < kCPerTile; ++h, ++cq) {
-              const int st = slot(kBarC, kCStages, cq, kCStage);
-              if (st < 0) return false;
-              tma_load_3d(smem + st * kCStage, &tm_q, &bar[B_FULL + kBarC + st], 0, qrow0, 4 * h);
-            }
+          const int qrow0 = ti.b * SH + rb * 128;
+          if (ti.first) {  // the segment's query rows: blocks 0..3 now, 4..7 after the tile's first c box
+            const int st = slot(kBarC, kCStages, cq++, kCStage);
+            if (st < 0) return false;
+            tma_load_3d(smem + st * kCStage, &tm_q, &bar[B_FULL + kBarC + st], 0, qrow0, 0);
             if (!mbar_wait(&bar[B_QREMPTY], ((uint32_t)ti.k & 1u) ^ 1u, wc)) return false;
             mbar_arrive_expect_tx(&bar[B_QRFULL], kBlk0);
             qr_last = ti.k;
@@ -573,6 +575,11 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             tma_load_2d(smem + kOffR + st * kRStage, &tm_kr, &bar[B_FULL + kBarR + st], 0, row0);
           }
           for (int h = 0; h < kCPerTile; ++h, ++cq) {
+            if (ti.first && h == 1) {  // the query rows' second half, between the tile's two c boxes
+              const int st = slot(kBarC, kCStages, cq++, kCStage);
+              if (st < 0) return false;
+              tma_load_3d(smem + st * kCStage, &tm_q, &bar[B_FULL + kBarC + st], 0, qrow0, 4);
+            }
             const int st = slot(kBarC, kCStages, cq, kCStage);
             if (st < 0) return false;
             if (h == 0) MLA_TRACE(p, TR_TMA_ISSUE, ti.i);
@@ -602,26 +609,33 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     if (lane == 0) {
       if (rank == 0) {
         constexpr uint32_t idesc = idesc_bf16_f32(128, kTok, 0, 0);
+        int ci = 0, ck = 0;  // the tile and segment whose q~ is being copied
+        // Half h of the segment's q~ (its c-ring stage) into tensor memory.
+        auto copy_q = [&](int h) -> bool {
+          const int q = cpos_q(ci, ck, h), st = q % kCStages;
+          if (!mbar_wait(&bar[B_FULL + kBarC + st], (uint32_t)(q / kCStages) & 1u, wc)) return false;
+          tc_fence_after();
+          const uint32_t sbase = smem_u32(smem + st * kCStage);
+#pragma unroll
+          for (int kk = 0; kk < 16; ++kk)  // 4 blocks x 4 slices of 16 columns
+            tmem_cp_128x256b(tmem + kQCol + (uint32_t)(h * 16 + kk) * 8,
+                             smem_desc(sbase + (kk >> 2) * kBlk0 + (kk & 3) * 32, 16, 1024, 2));
+          mma_commit(&bar[B_EMPTY + kBarC + st]);  // the stage is free once the copy has read it
+          return true;
+        };
         for_each_tile(p, g, *plan, [&](const TileInfo& ti) {
+          ci = ti.i;
+          ck = ti.k;
           const int sb = ti.i & 1;                            // S buffer of this tile
           const uint32_t sph = (uint32_t)(ti.i >> 1) & 1u;    // its phase
           if (ti.first) {
             // q~ of the segment: its two c stages go into tensor memory by
             // tcgen05.cp, after every MMA of the previous segment (which read
-            // the old q~) has completed; the copy is ordered before this
-            // thread's next MMAs.  q^R must have landed in its buffer.
+            // the old q~) has completed; a copy is ordered before this
+            // thread's next MMAs.  Half 0 now, half 1 after the MMAs of the
+            // tile's first c stage.  q^R must have landed in its buffer.
             if (ti.k > 0 && !mbar_wait(&bar[B_QREMPTY], (uint32_t)(ti.k - 1) & 1u, wc)) return false;
-            for (int h = 0; h < kCPerTile; ++h) {
-              const int q = cpos_q(ti.i, ti.k, h), st = q % kCStages;
-              if (!mbar_wait(&bar[B_FULL + kBarC + st], (uint32_t)(q / kCStages) & 1u, wc)) return false;
-              tc_fence_after();
-              const uint32_t sbase = smem_u32(smem + st * kCStage);
-#pragma unroll
-              for (int kk = 0; kk < 16; ++kk)  // 4 blocks x 4 slices of 16 columns
-                tmem_cp_128x256b(tmem + kQCol + (uint32_t)(h * 16 + kk) * 8,
-                                 smem_desc(sbase + (kk >> 2) * kBlk0 + (kk & 3) * 32, 16, 1024, 2));
-              mma_commit(&bar[B_EMPTY + kBarC + st]);  // the stage is free once the copy has read it
-            }
+            if (!copy_q(0)) return false;
             if (!mbar_wait(&bar[B_QRFULL], (uint32_t)ti.k & 1u, wc)) return false;
           }
           if (!mbar_wait(&bar[B_SEMPTY + sb], sph ^ 1u, wc)) return false;
@@ -639,7 +653,10 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             mma_commit(&bar[B_EMPTY + kBarR + st]);
           }
           for (int h = 0; h < kCPerTile; ++h) {  // c blocks 4h .. 4h + 3 against q~ from tensor memory
-            const int q = cpos_kv(ti.i, ti.k, h), st = q % kCStages;
+            // the second half of a new segment's q~ lands between the tile's c boxes;
+            // its copy writes columns the first half's MMAs do not read
+            if (ti.first && h == 1 && !copy_q(1)) return false;
+            const int q = cpos_kv(ti.i, ti.k, h, ti.first), st = q % kCStages;
             if (!mbar_wait(&bar[B_FULL + kBarC + st], (uint32_t)(q / kCStages) & 1u, wc)) return false;
             if (h == kCPerTile - 1) MLA_TRACE(p, TR_QK_LAST, ti.i);
             tc_fence_after();
