@@ -19,15 +19,16 @@
 // CTAs work on a few heads at a time and a head's expanded keys and values
 // are read from HBM about once and then from L2.
 //
-// Per CTA (256 threads): warp 0 issues the TMA copies of Q (once per item:
+// Per CTA (384 threads): warp 0 issues the TMA copies of Q (once per item:
 // q^C and q^R as three 128-byte-swizzle atoms) and of each key tile (k^C,
 // k^R), warp 2 those of each value tile (v^C), warp 1 issues the MMAs (one
-// thread), warps 4..7 run the online softmax, one row per thread, and the
-// epilogue; warp 3 only takes part in set-up and wind-down.
+// thread), warps 4..11 run the online softmax and the epilogue, two threads
+// per row (one per 64-column half of the scores and of O); warp 3 only takes
+// part in set-up and wind-down.
 // Tensor memory holds three 128-column score buffers S and the 128 x 128 fp32
-// output O (columns 384..511).  QK^T runs two tiles ahead of the softmax; the softmax writes P (bf16) over the first half of each
-// 64-column half of its S buffer and P.V reads it from there (A operand in
-// tensor memory).  The online softmax keeps an integer reference exponent per
+// output O (columns 384..511).  QK^T runs two tiles ahead of the softmax; the
+// softmax writes P (bf16) over the first half of each 64-column half of its
+// S buffer and P.V reads it from there (A operand in tensor memory).  The online softmax keeps an integer reference exponent per
 // row (log2 units) that moves only when a tile's maximum passes it by more
 // than 8, so every rescale of O and of the row sum is an exact power of two.
 #pragma once
@@ -36,7 +37,7 @@
 
 namespace mla {
 
-constexpr int kPfThreads = 256;
+constexpr int kPfThreads = 384;
 constexpr int kPfAtom = 128 * 128;  // 128 rows x 64 bf16 columns (one swizzle atom column), 16 KB
 constexpr int kPfQ = 3 * kPfAtom;   // q^C (two atoms) + q^R (one)
 constexpr int kPfK = 3 * kPfAtom;   // k^C (two atoms) + k^R (one)
@@ -48,9 +49,17 @@ constexpr int kPfOffV = kPfOffK + kPfKStages * kPfK;
 constexpr int kPfOffBar = kPfOffV + kPfVStages * kPfV;
 enum : int {
   PF_QFULL = 0, PF_QEMPTY = 1, PF_KFULL = 2, PF_KEMPTY = 4, PF_VFULL = 6, PF_VEMPTY = 8,
-  PF_SFULL = 10, PF_PREADY = 13, PF_PVDONE = 16, PF_OFREE = 19, PF_DRAIN = 20, PF_NBARS = 21
+  PF_SFULL = 10, PF_PREADY = 13, PF_PVDONE = 16, PF_OFREE = 19, PF_DRAIN = 20,
+  PF_XCH = 21,   // row-maximum exchange of a row's two threads [tile parity][quadrant]
+  PF_XL = 29,    // row-sum exchange at an item's end [quadrant]
+  PF_NBARS = 33
 };
-constexpr size_t kPfSmem = (size_t)kPfOffBar + PF_NBARS * 8 + 16;
+// the two threads of a row exchange partial row maxima [tile parity][half][row]
+// and, at an item's end, partial row sums [half][row]
+constexpr int kPfOffXch = kPfOffBar + PF_NBARS * 8 + 16;
+constexpr int kPfXchBytes = 2 * 2 * 128 * 4 + 2 * 128 * 4;
+constexpr size_t kPfSmem = (size_t)kPfOffXch + kPfXchBytes;
+static_assert(kPfSmem <= 232448, "prefill shared memory exceeds 227 KB");
 constexpr uint32_t kPfOCol = 384;  // O; the score buffers sit at columns 0, 128 and 256
 
 struct PrefillParams {
@@ -159,8 +168,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   if (threadIdx.x == 0) {
     *abort_flag = 0u;
     for (int i = 0; i < PF_NBARS; ++i) {
-      const bool per_thread = (i >= PF_PREADY && i < PF_PREADY + 3) || i == PF_OFREE;
-      mbar_init(&bar[i], per_thread ? 128u : 1u);
+      uint32_t n = 1;  // TMA arrivals and MMA commits
+      if ((i >= PF_PREADY && i < PF_PREADY + 3) || i == PF_OFREE) n = 256;  // every row thread
+      if (i >= PF_XCH && i < PF_NBARS) n = 64;                              // the two warps of a quadrant
+      mbar_init(&bar[i], n);
     }
     fence_mbar_init_cluster();
     tma_prefetch_desc(&tm_qn);
@@ -319,10 +330,17 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     }
   } else if (warp >= 4) {
     // -------------------------------------------------------------- softmax + epilogue
-    const int q4 = warp & 3;
+    // Two threads per row (warps 4..7: score columns 0..63, warps 8..11:
+    // 64..127, of the rows of tensor-memory quadrant warp & 3).  They
+    // exchange partial row maxima per tile and partial row sums per item
+    // through shared memory and mbarriers, so both take the same reference
+    // exponent; each rescales and writes its own 64 columns of O.
+    const int q4 = warp & 3, hw = (warp - 4) >> 2;
     const int r = q4 * 32 + lane;  // this thread's row = tensor-memory lane
     const uint32_t tl = tmem + ((uint32_t)(q4 * 32) << 16);
-    uint32_t g = 0;
+    float* xmax = reinterpret_cast<float*>(smem + kPfOffXch);  // [parity][half][row]
+    float* xsum = xmax + 2 * 2 * 128;                          // [half][row]
+    uint32_t g = 0, it = 0;
     bool ok = true;
     PfIter iter;
     PfItem ii;
@@ -331,35 +349,44 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       const int pr = min(ii.p0 + r, ii.p_last);  // rows past the block's last query repeat it
       float m_ref = -INFINITY, l = 0.f;
       for (int t = 0; t < ii.nt; ++t) {
-        const uint32_t sb = g % 3;
+        const uint32_t sb = g % 3, par = g & 1u;
         if (!pf_warp_wait(&bar[PF_SFULL + sb], (g / 3) & 1u, wc)) {
           ok = false;
           break;
         }
-        if (r == 0) PF_TRACE(p, PT_SREADY, g);
+        if (r == 0 && hw == 0) PF_TRACE(p, PT_SREADY, g);
         tc_fence_after();
-        const uint32_t sc = tl + sb * 128;
-        const int nv = min(max(pr + 1 - t * 128, 0), 128);
-        // the row's 128 scores, read from tensor memory once
-        uint32_t v[128];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(sc + (uint32_t)(c * 32), *reinterpret_cast<uint32_t(*)[32]>(&v[c * 32]));
+        const uint32_t sc = tl + sb * 128 + (uint32_t)(hw * 64);
+        // visible columns of this thread's half
+        const int nv = min(max(pr + 1 - t * 128 - hw * 64, 0), 64);
+        uint32_t v[64];
+        tmem_ld32(sc, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+        tmem_ld32(sc + 32u, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
         tmem_wait_ld();
-        const bool full = __all_sync(0xffffffffu, nv == 128);  // no column of this warp's rows is masked
-        // row maximum over eight independent partial maxima (short dependency chains)
+        const bool full = __all_sync(0xffffffffu, nv == 64);  // no column of this warp's half is masked
         float pm[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) pm[k] = -INFINITY;
         if (full) {
 #pragma unroll
-          for (int u = 0; u < 128; ++u) pm[u & 7] = fmaxf(pm[u & 7], __uint_as_float(v[u]));
+          for (int u = 0; u < 64; ++u) pm[u & 7] = fmaxf(pm[u & 7], __uint_as_float(v[u]));
         } else {
 #pragma unroll
-          for (int u = 0; u < 128; ++u)
+          for (int u = 0; u < 64; ++u)
             if (u < nv) pm[u & 7] = fmaxf(pm[u & 7], __uint_as_float(v[u]));
         }
         float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])), fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
-        mx *= p.scale_log2;
+        // the row's maximum over both halves
+        xmax[(par * 2 + hw) * 128 + r] = mx;
+        mbar_arrive(&bar[PF_XCH + par * 4 + q4]);
+        if (!mbar_wait(&bar[PF_XCH + par * 4 + q4], (g >> 1) & 1u, wc)) {
+          ok = false;
+        }
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        mx = fmaxf(mx, xmax[(par * 2 + (hw ^ 1)) * 128 + r]) * p.scale_log2;
         const float cm = ceilf(mx);
         int ex = 0;  // O and l are rescaled by 2^-ex; 255 stands for 0
         if (cm > m_ref + 8.f) {
@@ -378,9 +405,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           tc_fence_after();
           const float alpha = ex == 255 ? 0.f : pf_exp2_int(-ex);
 #pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
+          for (int c = 0; c < 2; ++c) {
             uint32_t o[32];
-            const uint32_t a = tl + kPfOCol + (uint32_t)(c * 32);
+            const uint32_t a = tl + kPfOCol + (uint32_t)(hw * 64 + c * 32);
             tmem_ld32(a, o);
             tmem_wait_ld();
             if (need) {
@@ -391,48 +418,49 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           }
         }
         // P = 2^(s scale log2 e - m) in bf16, written over the first 32
-        // columns of each 64-column half (already read above)
+        // columns of this thread's 64-column half (already read above)
         float lsa[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) lsa[k] = 0.f;
+        uint32_t pk[32];
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          uint32_t pk[32];
-#pragma unroll
-          for (int u = 0; u < 32; ++u) {
-            const int col = hf * 64 + 2 * u;
-            float e0 = ex2_approx(fmaf(__uint_as_float(v[col]), p.scale_log2, -mu));
-            float e1 = ex2_approx(fmaf(__uint_as_float(v[col + 1]), p.scale_log2, -mu));
-            if (!full) {
-              e0 = col < nv ? e0 : 0.f;
-              e1 = col + 1 < nv ? e1 : 0.f;
-            }
-            pk[u] = pack_bf16x2(e0, e1);
-            // the row sum adds exactly the bf16 weights that P.V multiplies
-            lsa[(2 * u) & 7] += __uint_as_float(pk[u] << 16);
-            lsa[(2 * u + 1) & 7] += __uint_as_float(pk[u] & 0xffff0000u);
+        for (int u = 0; u < 32; ++u) {
+          float e0 = ex2_approx(fmaf(__uint_as_float(v[2 * u]), p.scale_log2, -mu));
+          float e1 = ex2_approx(fmaf(__uint_as_float(v[2 * u + 1]), p.scale_log2, -mu));
+          if (!full) {
+            e0 = 2 * u < nv ? e0 : 0.f;
+            e1 = 2 * u + 1 < nv ? e1 : 0.f;
           }
-          tmem_st32(sc + (uint32_t)(hf * 64), pk);
+          pk[u] = pack_bf16x2(e0, e1);
+          // the row sum adds exactly the bf16 weights that P.V multiplies
+          lsa[(2 * u) & 7] += __uint_as_float(pk[u] << 16);
+          lsa[(2 * u + 1) & 7] += __uint_as_float(pk[u] & 0xffff0000u);
         }
+        tmem_st32(sc, pk);
         const float ls = ((lsa[0] + lsa[1]) + (lsa[2] + lsa[3])) + ((lsa[4] + lsa[5]) + (lsa[6] + lsa[7]));
         tmem_wait_st();
         l += ls;
         tc_fence_before();
         mbar_arrive(&bar[PF_PREADY + sb]);
-        if (r == 0) PF_TRACE(p, PT_PREADY, g);
+        if (r == 0 && hw == 0) PF_TRACE(p, PT_PREADY, g);
         ++g;
       }
       if (!ok) break;
-      // epilogue: out = O / l once the item's last P.V has completed
+      // epilogue: out = O / l once the item's last P.V has completed, l the
+      // sum of both halves' partial sums
+      xsum[hw * 128 + r] = l;
+      mbar_arrive(&bar[PF_XL + q4]);
+      if (!pf_warp_wait(&bar[PF_XL + q4], it & 1u, wc)) break;
+      l += xsum[(hw ^ 1) * 128 + r];
       if (!pf_warp_wait(&bar[PF_PVDONE + (g - 1) % 3], ((g - 1) / 3) & 1u, wc)) break;
       tc_fence_after();
       const float inv = 1.f / l;
       const bool valid = r < ii.nrow;
-      uint4* orow = reinterpret_cast<uint4*>(p.out + (((size_t)ii.b * p.S + ii.s0 + r) * p.H + ii.h) * 128);
+      uint4* orow = reinterpret_cast<uint4*>(p.out + (((size_t)ii.b * p.S + ii.s0 + r) * p.H + ii.h) * 128 + hw * 64);
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t v[32];
-        tmem_ld32(tl + kPfOCol + (uint32_t)(c * 32), v);
+        tmem_ld32(tl + kPfOCol + (uint32_t)(hw * 64 + c * 32), v);
         tmem_wait_ld();
         uint32_t o[16];
 #pragma unroll
@@ -445,6 +473,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       }
       tc_fence_before();
       mbar_arrive(&bar[PF_OFREE]);
+      ++it;
     }
   }
 
