@@ -256,12 +256,15 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         if (!mbar_wait(&bar[PF_KFULL + st], (kc / kPfKStages) & 1u, wc)) return false;
         PF_TRACE(p, PT_KFULL, gg);
         tc_fence_after();
-        const uint32_t qa = smem_u32(smem), ka = smem_u32(smem + kPfOffK + st * kPfK);
+        // descriptors built once and stepped (a descriptor's start address is
+        // its low field, in 16-byte units, and stays below 2^14 here)
+        const uint64_t qd = smem_desc(smem_u32(smem), 16, 1024, 2);
+        const uint64_t kd = smem_desc(smem_u32(smem + kPfOffK + st * kPfK), 16, 1024, 2);
+        const uint32_t sd = tmem + sb * 128;
 #pragma unroll
         for (int kk = 0; kk < 12; ++kk) {  // 192 = 3 atoms x 4 K-steps of 16
-          const uint32_t off = (uint32_t)((kk >> 2) * kPfAtom + (kk & 3) * 32);
-          mma_ss(tmem + sb * 128, smem_desc(qa + off, 16, 1024, 2), smem_desc(ka + off, 16, 1024, 2), idq,
-                 kk > 0 ? 1u : 0u);
+          const uint64_t off = (uint64_t)(((kk >> 2) * kPfAtom + (kk & 3) * 32) >> 4);
+          mma_ss(sd, qd + off, kd + off, idq, kk > 0 ? 1u : 0u);
         }
         mma_commit(&bar[PF_KEMPTY + st]);
         mma_commit(&bar[PF_SFULL + sb]);
@@ -304,12 +307,13 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                   *reinterpret_cast<uint4*>(vb + a * kPfAtom + row * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
             fence_proxy_async_cta();
           }
-          const uint32_t vba = smem_u32(vb);
-          for (int kk = 0; kk < nk; ++kk) {
-            const uint32_t pa = tmem + sb * 128 + (uint32_t)((kk >> 2) * 64 + (kk & 3) * 8);
-            mma_ts(tmem + kPfOCol, pa, smem_desc(vba + (uint32_t)kk * 2048, kPfAtom, 1024, 2), idv,
-                   (t > 0 || kk > 0) ? 1u : 0u);
-          }
+          const uint64_t vd = smem_desc(smem_u32(vb), kPfAtom, 1024, 2);
+          const uint32_t pa = tmem + sb * 128, od = tmem + kPfOCol, acc0 = t > 0 ? 1u : 0u;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)  // up to 8 K-steps of 16 keys: 2048 bytes of V each
+            if (kk < nk)
+              mma_ts(od, pa + (uint32_t)((kk >> 2) * 64 + (kk & 3) * 8), vd + (uint64_t)(kk * 128), idv,
+                     kk > 0 ? 1u : acc0);
           mma_commit(&bar[PF_VEMPTY + st]);
           mma_commit(&bar[PF_PVDONE + sb]);
           PF_TRACE(p, PT_PV, g);
