@@ -144,13 +144,15 @@ __global__ void __launch_bounds__(kExThreads, 1)
               break;
             }
             tc_fence_after();
-            const uint32_t b0 = smem_u32(smem + kExOffB + st * kExB);
+            // descriptors built once and stepped (the start address is the low
+            // field, in 16-byte units; every address here is below 2^18)
+            const uint64_t bd = smem_desc(smem_u32(smem + kExOffB + st * kExB), 16, 1024, 2);
+            const uint64_t ad = smem_desc(a0 + (uint32_t)(ks * 2 * kExAtom), 16, 1024, 2);
+            const uint32_t dd = tmem + buf * 128;
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {  // two atoms x four K-steps of 16
-              const uint32_t aoff = (uint32_t)((ks * 2 + (kk >> 2)) * kExAtom + (kk & 3) * 32);
-              const uint32_t boff = (uint32_t)((kk >> 2) * kExAtom + (kk & 3) * 32);
-              mma_ss(tmem + buf * 128, smem_desc(a0 + aoff, 16, 1024, 2), smem_desc(b0 + boff, 16, 1024, 2),
-                     idesc, (ks > 0 || kk > 0) ? 1u : 0u);
+              const uint64_t off = (uint64_t)((((kk >> 2) * kExAtom) + (kk & 3) * 32) >> 4);
+              mma_ss(dd, ad + off, bd + off, idesc, (ks > 0 || kk > 0) ? 1u : 0u);
             }
             mma_commit(&bar[EX_BEMPTY + st]);
           }
