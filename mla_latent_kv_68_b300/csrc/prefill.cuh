@@ -21,12 +21,12 @@
 //
 // Per CTA (384 threads): warp 0 issues the TMA copies of Q (once per item:
 // q^C and q^R as three 128-byte-swizzle atoms) and of each key tile (k^C,
-// k^R), warp 2 those of each value tile (v^C), warp 1 issues the MMAs (one
-// thread), warps 4..11 run the online softmax and the epilogue, two threads
-// per row (one per 64-column half of the scores and of O); warp 3 only takes
-// part in set-up and wind-down.
+// k^R), warp 2 those of each value tile (v^C); one thread of warp 1 issues
+// the QK^T MMAs and one of warp 3 the P.V MMAs; warps 4..11 run the online
+// softmax and the epilogue, two threads per row (one per 64-column half of
+// the scores and of O).
 // Tensor memory holds three 128-column score buffers S and the 128 x 128 fp32
-// output O (columns 384..511).  QK^T runs two tiles ahead of the softmax; the
+// output O (columns 384..511).  QK^T runs up to three tiles ahead of P.V; the
 // softmax writes P (bf16) over the first half of each 64-column half of its
 // S buffer and P.V reads it from there (A operand in tensor memory).  The online softmax keeps an integer reference exponent per
 // row (log2 units) that moves only when a tile's maximum passes it by more
@@ -52,7 +52,8 @@ enum : int {
   PF_SFULL = 10, PF_PREADY = 13, PF_PVDONE = 16, PF_OFREE = 19, PF_DRAIN = 20,
   PF_XCH = 21,   // row-maximum exchange of a row's two threads [tile parity][quadrant]
   PF_XL = 29,    // row-sum exchange at an item's end [quadrant]
-  PF_NBARS = 33
+  PF_DRAIN2 = 33,  // the P.V issuer's final drain
+  PF_NBARS = 34
 };
 // the two threads of a row exchange partial row maxima [tile parity][half][row]
 // and, at an item's end, partial row sums [half][row]
@@ -170,7 +171,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     for (int i = 0; i < PF_NBARS; ++i) {
       uint32_t n = 1;  // TMA arrivals and MMA commits
       if ((i >= PF_PREADY && i < PF_PREADY + 3) || i == PF_OFREE) n = 256;  // every row thread
-      if (i >= PF_XCH && i < PF_NBARS) n = 64;                              // the two warps of a quadrant
+      if (i >= PF_XCH && i < PF_DRAIN2) n = 64;                             // the two warps of a quadrant
       mbar_init(&bar[i], n);
     }
     fence_mbar_init_cluster();
@@ -242,44 +243,61 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      // ------------------------------------------------------------ MMA issuer
+      // ------------------------------------------------------ QK^T issuer
+      // Two threads issue the MMAs, each with its own commits: this one QK^T,
+      // warp 3's P.V (they write different tensor-memory columns, and the
+      // barriers order them), so neither waits behind the other's issue.
       constexpr uint32_t idq = idesc_bf16_f32(128, 128, 0, 0);  // S = Q K^T, both K-major
-      constexpr uint32_t idv = idesc_bf16_f32(128, 128, 0, 1);  // O += P V, V MN-major
-      uint32_t kc = 0, vc = 0, g = 0, it = 0;
+      uint32_t kc = 0, g = 0, it = 0;
       bool ok = true;
-      // QK^T of the tile with running index gg into score buffer gg % 3, whose
-      // previous P (tile gg - 3) must have been consumed by its P.V.
-      auto qk = [&](uint32_t gg) -> bool {
-        const uint32_t sb = gg % 3;
-        if (gg >= 3 && !mbar_wait(&bar[PF_PVDONE + sb], ((gg / 3) - 1) & 1u, wc)) return false;
-        const uint32_t st = kc % kPfKStages;
-        if (!mbar_wait(&bar[PF_KFULL + st], (kc / kPfKStages) & 1u, wc)) return false;
-        PF_TRACE(p, PT_KFULL, gg);
-        tc_fence_after();
-        // descriptors built once and stepped (a descriptor's start address is
-        // its low field, in 16-byte units, and stays below 2^14 here)
-        const uint64_t qd = smem_desc(smem_u32(smem), 16, 1024, 2);
-        const uint64_t kd = smem_desc(smem_u32(smem + kPfOffK + st * kPfK), 16, 1024, 2);
-        const uint32_t sd = tmem + sb * 128;
-#pragma unroll
-        for (int kk = 0; kk < 12; ++kk) {  // 192 = 3 atoms x 4 K-steps of 16
-          const uint64_t off = (uint64_t)(((kk >> 2) * kPfAtom + (kk & 3) * 32) >> 4);
-          mma_ss(sd, qd + off, kd + off, idq, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(&bar[PF_KEMPTY + st]);
-        mma_commit(&bar[PF_SFULL + sb]);
-        PF_TRACE(p, PT_QK, gg);
-        ++kc;
-        return true;
-      };
       PfIter iter;
       PfItem ii;
       while (ok && iter.next(p, ii)) {
         if (!ii.ok) continue;
-        // QK^T runs two tiles ahead of P.V: while the softmax works on tile t,
-        // the scores of tiles t + 1 and t + 2 are computed or ready
-        if (!mbar_wait(&bar[PF_QFULL], it & 1u, wc) || !qk(g) || (ii.nt > 1 && !qk(g + 1))) break;
-        if (ii.nt <= 2) mma_commit(&bar[PF_QEMPTY]);  // Q is free once these QK^T are done
+        if (!mbar_wait(&bar[PF_QFULL], it & 1u, wc)) break;
+        for (int t = 0; t < ii.nt; ++t, ++g) {
+          // QK^T of tile g into score buffer g % 3, whose previous P (tile
+          // g - 3) must have been consumed by its P.V
+          const uint32_t sb = g % 3, st = kc % kPfKStages;
+          if ((g >= 3 && !mbar_wait(&bar[PF_PVDONE + sb], ((g / 3) - 1) & 1u, wc)) ||
+              !mbar_wait(&bar[PF_KFULL + st], (kc / kPfKStages) & 1u, wc)) {
+            ok = false;
+            break;
+          }
+          PF_TRACE(p, PT_KFULL, g);
+          tc_fence_after();
+          // descriptors built once and stepped (a descriptor's start address is
+          // its low field, in 16-byte units, and stays below 2^14 here)
+          const uint64_t qd = smem_desc(smem_u32(smem), 16, 1024, 2);
+          const uint64_t kd = smem_desc(smem_u32(smem + kPfOffK + st * kPfK), 16, 1024, 2);
+          const uint32_t sd = tmem + sb * 128;
+#pragma unroll
+          for (int kk = 0; kk < 12; ++kk) {  // 192 = 3 atoms x 4 K-steps of 16
+            const uint64_t off = (uint64_t)(((kk >> 2) * kPfAtom + (kk & 3) * 32) >> 4);
+            mma_ss(sd, qd + off, kd + off, idq, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(&bar[PF_KEMPTY + st]);
+          mma_commit(&bar[PF_SFULL + sb]);
+          PF_TRACE(p, PT_QK, g);
+          ++kc;
+        }
+        if (!ok) break;
+        mma_commit(&bar[PF_QEMPTY]);  // Q is free once the item's QK^T are done
+        ++it;
+      }
+      mma_commit(&bar[PF_DRAIN]);  // every MMA of this thread has finished before tensor memory is released
+      mbar_wait_drain(&bar[PF_DRAIN], 0, wc);
+    }
+  } else if (warp == 3) {
+    if (lane == 0) {
+      // -------------------------------------------------------- P.V issuer
+      constexpr uint32_t idv = idesc_bf16_f32(128, 128, 0, 1);  // O += P V, V MN-major
+      uint32_t vc = 0, g = 0, it = 0;
+      bool ok = true;
+      PfIter iter;
+      PfItem ii;
+      while (ok && iter.next(p, ii)) {
+        if (!ii.ok) continue;
         for (int t = 0; t < ii.nt; ++t) {
           const uint32_t sb = g % 3, st = vc % kPfVStages;
           if (!mbar_wait(&bar[PF_PREADY + sb], (g / 3) & 1u, wc) ||
@@ -319,18 +337,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           PF_TRACE(p, PT_PV, g);
           ++vc;
           ++g;
-          if (t + 2 < ii.nt) {  // tile t + 2 (running index g + 1) into the buffer P.V of t - 1 freed
-            if (!qk(g + 1)) {
-              ok = false;
-              break;
-            }
-            if (t + 3 == ii.nt) mma_commit(&bar[PF_QEMPTY]);
-          }
         }
         ++it;
       }
-      mma_commit(&bar[PF_DRAIN]);  // every MMA has finished before tensor memory is released
-      mbar_wait_drain(&bar[PF_DRAIN], 0, wc);
+      mma_commit(&bar[PF_DRAIN2]);  // every MMA of this thread has finished before tensor memory is released
+      mbar_wait_drain(&bar[PF_DRAIN2], 0, wc);
     }
   } else if (warp >= 4) {
     // -------------------------------------------------------------- softmax + epilogue
