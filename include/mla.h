@@ -59,7 +59,7 @@ typedef uint16_t mla_bf16; /* raw bf16 bit pattern */
 typedef enum {
   MLA_OK = 0,
   MLA_ERR_INVALID_ARG = 1, /* null pointer, misalignment, bad size or stride */
-  MLA_ERR_UNSUPPORTED = 2, /* a shape this build does not implement */
+  MLA_ERR_UNSUPPORTED = 2, /* a shape the library does not implement */
   MLA_ERR_WORKSPACE = 3,   /* workspace missing or too small */
   MLA_ERR_CUDA = 4,        /* a CUDA runtime call or a launch failed */
   MLA_ERR_BAD_SEQLEN = 5,  /* device: some seqlens[b] < S or > Lmax */
